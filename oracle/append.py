@@ -1,0 +1,92 @@
+"""Quantise-and-append of new K/V tokens into a paged cache (float64 oracle).
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).
+
+The pages name the KV write path only as a module imported next to the
+attention extension ("1Cat-vLLM", section on the source build / runtime
+notes: ``paged_kv_utils``) and fix two of its parameters: the cache stores FP8
+with static per-tensor scales that are never computed online ("1Cat-vLLM",
+"Optional experimental feature: FP8 KV cache": do not add
+``--calculate-kv-scales``), in pages of 2048 tokens ("SM70 release profile
+and acceleration status": 2048-token KV blocks) or 16 (its override table:
+``--block-size 16``). Everything else is a reading, stated here:
+
+* cache layout ``[num_blocks, Hkv, P, D]`` (one contiguous ``P x D`` chunk per
+  page and KV head), separate K and V pools;
+* token i goes to ``slot = slot_mapping[i]``, ``block = slot // P``,
+  ``offset = slot % P``; a negative slot means "skip this token";
+* the stored byte is ``encode(float32(float32(x16) / scale))``: the fp16 input
+  widened to float32, divided (not multiplied by a reciprocal) by the float32
+  scale with one IEEE round-to-nearest, then FP8 round-to-nearest-even with
+  saturation to the largest finite value;
+* an fp16 cache (no quantisation) stores the fp16 bits unchanged.
+
+The float32 quotient is formed as the float64 quotient rounded once to
+float32. That is the correctly rounded float32 quotient: for p-bit operands a
+2p+2-bit intermediate makes the second rounding innocuous, and float64 has
+53 >= 2*24+2 bits.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from . import fp8
+
+
+def quantise(x16: np.ndarray, scale: float, fmt) -> np.ndarray:
+    """uint8 codes of fp16 values divided by a float32 per-tensor scale."""
+    x32 = np.asarray(x16, dtype=np.float16).astype(np.float32)
+    s32 = np.float32(scale)
+    q = (x32.astype(np.float64) / np.float64(s32)).astype(np.float32)
+    return fp8.encode(q, fmt)
+
+
+def append(cache: np.ndarray, new: np.ndarray, slot_mapping: np.ndarray,
+           page_size: int, scale, kv_dtype: str) -> None:
+    """Write ``new[i]`` (fp16 ``[Hkv, D]``) into ``cache`` at ``slot_mapping[i]``.
+
+    ``cache`` is ``uint8 [num_blocks, Hkv, P, D]`` for ``kv_dtype`` in
+    ``{"e4m3", "e5m2"}`` or ``float16 [num_blocks, Hkv, P, D]`` for ``"fp16"``.
+    Updated in place. Tokens are visited in order, so a slot named twice ends
+    with the later token (the GPU path makes no promise there; tests never
+    repeat a slot).
+    """
+    new = np.asarray(new, dtype=np.float16)
+    n_tok = new.shape[0]
+    num_blocks = cache.shape[0]
+    for i in range(n_tok):
+        slot = int(slot_mapping[i])
+        if slot < 0:
+            continue
+        block, off = divmod(slot, page_size)
+        if block >= num_blocks:
+            raise IndexError(f"slot {slot} outside a pool of {num_blocks} pages")
+        if kv_dtype == "fp16":
+            cache[block, :, off, :] = new[i]
+        else:
+            cache[block, :, off, :] = quantise(new[i], scale, kv_dtype)
+
+
+def append_bulk(cache: np.ndarray, new: np.ndarray, slot_mapping: np.ndarray,
+                page_size: int, scale, kv_dtype: str) -> None:
+    """Same result as :func:`append` for distinct slots, vectorised over tokens.
+
+    Used to populate large caches; ``tests/test_oracle_append.py`` checks it
+    equals the token-by-token loop.
+    """
+    new = np.asarray(new, dtype=np.float16)
+    slots = np.asarray(slot_mapping, dtype=np.int64)
+    keep = slots >= 0
+    slots = slots[keep]
+    if slots.size == 0:
+        return
+    if np.any(slots // page_size >= cache.shape[0]):
+        raise IndexError("slot outside the pool")
+    block = slots // page_size
+    off = slots % page_size
+    vals = new[keep]
+    if kv_dtype != "fp16":
+        vals = quantise(vals, scale, kv_dtype)
+    # cache[block, :, off, :] with fancy indices on axes 0 and 2
+    cache[block, :, off, :] = vals
