@@ -1,0 +1,15 @@
+// Decode kernels for the e5m2 cache (head_dim 128/256 x 1 or 2 row tiles per warp).
+#include "decode_launch.cuh"
+
+namespace pfkv {
+
+cudaError_t launch_decode_e5m2(const DecodeLaunch& cfg, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+  return launch_decode_kv<kKvE5m2>(cfg, tmk, tmv, p, grid, stream);
+}
+
+int decode_smem_e5m2(const DecodeLaunch& cfg, int ncw) { return decode_smem_kv<kKvE5m2>(cfg, ncw); }
+
+int decode_ctas_e5m2(const DecodeLaunch& cfg, int ncw) { return decode_ctas_kv<kKvE5m2>(cfg, ncw); }
+
+}  // namespace pfkv

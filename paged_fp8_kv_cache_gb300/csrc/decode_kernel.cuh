@@ -1,0 +1,506 @@
+// Paged decode / grouped causal-verify attention over an FP8 (or fp16)
+// KV cache: the split-KV partial kernel.
+//
+// One CTA handles one (key range, KV head, sequence). Its rows are the
+// T * g query rows (query token t, head of the group) that share the KV
+// head -- one tile for ordinary GQA decode and for the grouped q8 verifier
+// ("1Cat-vLLM 1.5.0", "Flash-V100 long-context improvements": grouped q8
+// verifier, page-ID reuse, 128-bit cache loads, long-context split route).
+//
+// Warp roles:
+//  * one producer warp: walks the key range 64 keys at a time, reads each
+//    page id from the block table once and issues TMA tile copies of the K
+//    and V rows (FP8 bytes, 128-byte swizzle) into a ring of shared-memory
+//    stages, signalling an mbarrier per stage;
+//  * NRG x NTS consumer warps: row group rg (8*NT query rows) x token slice
+//    ts. Each consumer handles, per stage, the 16-key groups ts, ts+NTS, ...
+//    For a group it converts the FP8 K bytes to fp16 in registers (exact),
+//    computes S^T = K Q^T with mma.sync (16 keys x 8 rows x 16 dims per
+//    instruction, fp32 accumulate), masks by causal limit and sequence end,
+//    updates its running max / sum (online softmax, base-2 exponent), moves
+//    P^T into MMA operand form with movmatrix and accumulates O^T = V^T P^T
+//    with V converted in registers the same way.
+// At the end the NTS partial states of each row group are combined through
+// shared memory and written either as the final output (fp16 out + fp32
+// LSE) when the sequence has a single key range, or as a normalised fp32
+// partial plus its LSE for the merge kernel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "device_utils.cuh"
+#include "frag_layout.h"
+#include "pfkv_internal.h"
+
+namespace pfkv {
+
+template <int D, int KV>
+struct DecodeShape {
+  static constexpr int ELT = (KV == kKvFp16) ? 2 : 1;
+  static constexpr int ROWB = D * ELT;
+  static constexpr int NBOX = ROWB / kBoxBytes;
+  static constexpr int KV_STAGE = NBOX * kSubTileBytes;  // K (or V) bytes of one stage
+  static constexpr int STAGE = 2 * KV_STAGE;
+  static constexpr int NS = STAGE <= 32768 ? 4 : 2;      // pipeline depth
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int MTILES = D / 16;                  // PV m-tiles over the head dim
+};
+
+// Dynamic shared memory needed by one CTA (without the 1 KB alignment slack).
+template <int D, int KV, int NT>
+constexpr int decode_smem_bytes(int ncw) {
+  using S = DecodeShape<D, KV>;
+  const int obuf = ncw * 8 * NT * D * 4;
+  const int ring = S::NS * S::STAGE;
+  const int body = obuf > ring ? obuf : ring;
+  return body + ncw * 8 * NT * 8 /* m, l */ + 2 * S::NS * 8 /* barriers */;
+}
+
+template <int D, int KV, int NT>
+__global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  const DecodeParams p) {
+  using S = DecodeShape<D, KV>;
+  constexpr int ELT = S::ELT, NBOX = S::NBOX, NS = S::NS, KSTEPS = S::KSTEPS, MTILES = S::MTILES;
+  constexpr int ROWS_W = 8 * NT;  // query rows per consumer warp
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int ncw = p.nrg * p.nts;
+  const int R = p.T * p.G;
+
+  // sequence length, validated against what the block table can address
+  int N = p.seq_lens[b];
+  {
+    const int cap = min(p.max_seq_len, p.max_blocks * p.page_size);
+    if (N < 0 || N > cap) {
+      if (threadIdx.x == 0 && split == 0 && kvh == 0) atomicOr(p.err, kDevErrSeqLen);
+      N = N < 0 ? 0 : cap;
+    }
+  }
+  const int nsplit_b = N > 0 ? (N + p.split_tokens - 1) / p.split_tokens : 1;
+  if (split >= nsplit_b) return;
+  const int t0 = split * p.split_tokens;
+  const int t1 = min(N, t0 + p.split_tokens);
+  const int ntiles = t1 > t0 ? (t1 - t0 + kTileKeys - 1) / kTileKeys : 0;
+
+  const int body_bytes = decode_smem_bytes<D, KV, NT>(ncw) - ncw * ROWS_W * 8 - 2 * NS * 8;
+  float2* ml_buf = reinterpret_cast<float2*>(smem + body_bytes);  // [ncw][ROWS_W] (m, l)
+  uint64_t* full = reinterpret_cast<uint64_t*>(ml_buf + ncw * ROWS_W);
+  uint64_t* empty = full + NS;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], ncw);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------------ producer
+  if (warp == ncw) {
+    if (lane == 0 && ntiles > 0) {
+      prefetch_tensormap(&tmk);
+      prefetch_tensormap(&tmv);
+      const int P = p.page_size;
+      const int* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks;
+      bool ok = true;
+      for (int it = 0; it < ntiles && ok; ++it) {
+        const int s = it % NS;
+        if (it >= NS && !mbar_wait(&empty[s], ((it / NS) - 1) & 1)) {
+          atomicOr(p.err, kDevErrTimeout);
+          ok = false;
+          break;
+        }
+        unsigned char* kdst = smem + s * S::STAGE;
+        unsigned char* vdst = kdst + S::KV_STAGE;
+        const int tile_start = t0 + it * kTileKeys;
+        if (P >= kTileKeys) {
+          int blk = bt[tile_start >> p.page_shift];
+          if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
+            atomicOr(p.err, kDevErrBlockId);
+            blk = 0;
+          }
+          const int row = (blk * p.num_kv_heads + kvh) * P + (tile_start & (P - 1));
+          mbar_arrive_expect_tx(&full[s], 2 * S::KV_STAGE);
+#pragma unroll
+          for (int bx = 0; bx < NBOX; ++bx) {
+            tma_load_2d(kdst + bx * kSubTileBytes, &tmk, &full[s], bx * (kBoxBytes / ELT), row);
+            tma_load_2d(vdst + bx * kSubTileBytes, &tmv, &full[s], bx * (kBoxBytes / ELT), row);
+          }
+        } else {
+          const int valid = min(kTileKeys, t1 - tile_start);
+          const int npages = (valid + P - 1) >> p.page_shift;
+          mbar_arrive_expect_tx(&full[s], 2 * NBOX * npages * P * kBoxBytes);
+          const int pfirst = tile_start >> p.page_shift;
+          for (int pg = 0; pg < npages; ++pg) {
+            int blk = bt[pfirst + pg];
+            if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
+              atomicOr(p.err, kDevErrBlockId);
+              blk = 0;
+            }
+            const int row = (blk * p.num_kv_heads + kvh) * P;
+#pragma unroll
+            for (int bx = 0; bx < NBOX; ++bx) {
+              tma_load_2d(kdst + bx * kSubTileBytes + pg * P * kBoxBytes, &tmk, &full[s], bx * (kBoxBytes / ELT), row);
+              tma_load_2d(vdst + bx * kSubTileBytes + pg * P * kBoxBytes, &tmv, &full[s], bx * (kBoxBytes / ELT), row);
+            }
+          }
+        }
+      }
+      // do not leave while copies may still land in this CTA's shared memory
+      const int first_pending = max(0, ntiles - NS);
+      for (int it = first_pending; it < ntiles; ++it) {
+        if (!mbar_wait(&full[it % NS], (it / NS) & 1)) {
+          atomicOr(p.err, kDevErrTimeout);
+          break;
+        }
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int rg = warp / p.nts, ts = warp % p.nts;
+  const int g8 = lane >> 2, c = lane & 3;
+  const int row_base = rg * ROWS_W;
+
+  float kscale = 1.f, vscale = 1.f;
+  if (KV != kKvFp16) {
+    kscale = *p.k_scale;
+    vscale = *p.v_scale;
+  }
+  // logits in base-2 units: s2 = acc * softmax_scale * k_scale * log2(e)
+  const float sc2 = p.softmax_scale * kscale * 1.4426950408889634f;
+
+  // Q^T fragments (B operand of S^T = K Q^T), kept in registers.
+  uint32_t qf[KSTEPS][NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int row = row_base + nt * 8 + g8;
+    const __half* qrow = nullptr;
+    if (row < R) {
+      const int t = row / p.G, j = row - t * p.G;
+      qrow = p.q + ((static_cast<size_t>(b) * p.T + t) * p.num_q_heads + kvh * p.G + j) * D;
+    }
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+      if (qrow) {
+        const uint2 v = *reinterpret_cast<const uint2*>(qrow + qk_elem(ELT, ks, c));
+        qf[ks][nt][0] = v.x;
+        qf[ks][nt][1] = v.y;
+      } else {
+        qf[ks][nt][0] = qf[ks][nt][1] = 0u;
+      }
+    }
+  }
+
+  // causal limit of the two rows (2c, 2c+1) of every n-tile this lane accumulates
+  int lim[NT][2];
+  int min_lim = INT_MAX;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int row = row_base + nt * 8 + 2 * c + e;
+      const int t = row / p.G;  // rows past R get t >= T: limited by N only
+      lim[nt][e] = min(N - 1, N - p.T + t);
+      if (row < R) min_lim = min(min_lim, lim[nt][e]);
+    }
+#pragma unroll
+  for (int off = 1; off < 4; off <<= 1) min_lim = min(min_lim, __shfl_xor_sync(0xffffffffu, min_lim, off));
+
+  float o[MTILES][NT][4];
+#pragma unroll
+  for (int i = 0; i < MTILES; ++i)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[i][nt][k] = 0.f;
+  float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      m_run[nt][e] = -CUDART_INF_F;
+      l_run[nt][e] = 0.f;
+    }
+
+  bool alive = true;
+  const int groups_per_stage = kTileKeys / 16;
+  for (int it = 0; it < ntiles; ++it) {
+    const int s = it % NS;
+    if (!mbar_wait(&full[s], (it / NS) & 1)) {
+      if (lane == 0) atomicOr(p.err, kDevErrTimeout);
+      alive = false;
+      break;
+    }
+    const unsigned char* Ks = smem + s * S::STAGE;
+    const unsigned char* Vs = Ks + S::KV_STAGE;
+    const int tile_start = t0 + it * kTileKeys;
+    const int valid = min(kTileKeys, t1 - tile_start);
+
+    for (int grp = ts; grp < groups_per_stage; grp += p.nts) {
+      if (grp * 16 >= valid) break;
+      const int key0 = tile_start + grp * 16;  // absolute position of key row 0 of this group
+
+      // ---- S^T = K Q^T
+      float sacc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sacc[nt][k] = 0.f;
+      const int r0 = grp * 16 + g8;
+#pragma unroll
+      for (int bx = 0; bx < NBOX; ++bx) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const unsigned char* kb = Ks + bx * kSubTileBytes;
+          const uint4 k0 = lds128(kb + swz_offset(r0, k_chunk(c, h)));
+          const uint4 k1 = lds128(kb + swz_offset(r0 + 8, k_chunk(c, h)));
+          const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w};
+          const uint32_t w1[4] = {k1.x, k1.y, k1.z, k1.w};
+          if constexpr (ELT == 1) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const int ks = (2 * bx + h) * 4 + w;
+              uint32_t a0, a1, a2, a3;
+              if constexpr (KV == kKvE4m3) {
+                a0 = e4m3x2_to_f16x2(w0[w]);
+                a1 = e4m3x2_to_f16x2(w1[w]);
+                a2 = e4m3x2_to_f16x2(w0[w] >> 16);
+                a3 = e4m3x2_to_f16x2(w1[w] >> 16);
+              } else {
+                a0 = e5m2_bytes_to_f16x2<0, 1>(w0[w]);
+                a1 = e5m2_bytes_to_f16x2<0, 1>(w1[w]);
+                a2 = e5m2_bytes_to_f16x2<2, 3>(w0[w]);
+                a3 = e5m2_bytes_to_f16x2<2, 3>(w1[w]);
+              }
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) mma_16816(sacc[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int ks = (2 * bx + h) * 2 + u;
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                mma_16816(sacc[nt], w0[2 * u], w1[2 * u], w0[2 * u + 1], w1[2 * u + 1], qf[ks][nt][0], qf[ks][nt][1]);
+            }
+          }
+        }
+      }
+
+      // ---- scale, mask, running max
+      const bool need_mask = (key0 + 15 > min_lim);
+      const int keyA = key0 + g8, keyB = keyA + 8;
+      float mx[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float sa = sacc[nt][e] * sc2, sb = sacc[nt][2 + e] * sc2;
+          if (need_mask) {
+            if (keyA > lim[nt][e]) sa = -CUDART_INF_F;
+            if (keyB > lim[nt][e]) sb = -CUDART_INF_F;
+          }
+          sacc[nt][e] = sa;
+          sacc[nt][2 + e] = sb;
+          mx[nt][e] = fmaxf(sa, sb);
+        }
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) mx[nt][e] = fmaxf(mx[nt][e], __shfl_xor_sync(0xffffffffu, mx[nt][e], off));
+
+      bool changed = false;
+      float alpha[NT][2], muse[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float mnew = fmaxf(m_run[nt][e], mx[nt][e]);
+          muse[nt][e] = (mnew == -CUDART_INF_F) ? 0.f : mnew;
+          alpha[nt][e] = fast_exp2(m_run[nt][e] - muse[nt][e]);  // 0 when the old max was -inf
+          changed |= (mnew != m_run[nt][e]);
+          m_run[nt][e] = mnew;
+        }
+      if (__any_sync(0xffffffffu, changed)) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            l_run[nt][e] *= alpha[nt][e];
+#pragma unroll
+            for (int i = 0; i < MTILES; ++i) {
+              o[i][nt][e] *= alpha[nt][e];
+              o[i][nt][2 + e] *= alpha[nt][e];
+            }
+          }
+      }
+
+      // ---- P = exp2(s - m), then P^T fragments via movmatrix
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float pv[4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          pv[e] = fast_exp2(sacc[nt][e] - muse[nt][e]);
+          pv[2 + e] = fast_exp2(sacc[nt][2 + e] - muse[nt][e]);
+          l_run[nt][e] += pv[e] + pv[2 + e];
+        }
+        pb[nt][0] = movmatrix_trans(pack_half2(pv[0], pv[1]));  // keys 0..7 of the group
+        pb[nt][1] = movmatrix_trans(pack_half2(pv[2], pv[3]));  // keys 8..15
+      }
+
+      // ---- O^T += V^T P^T
+      const bool v_tail = (grp * 16 + 16 > valid);
+#pragma unroll
+      for (int bx = 0; bx < NBOX; ++bx) {
+        const unsigned char* vb = Vs + bx * kSubTileBytes;
+        uint4 vr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = grp * 16 + pv_key(c, i);
+          vr[i] = lds128(vb + swz_offset(r, g8));
+          if (v_tail && (r >= valid)) vr[i] = make_uint4(0u, 0u, 0u, 0u);  // stale bytes past the sequence end
+        }
+        const uint32_t W0[4] = {vr[0].x, vr[0].y, vr[0].z, vr[0].w};
+        const uint32_t W1[4] = {vr[1].x, vr[1].y, vr[1].z, vr[1].w};
+        const uint32_t W2[4] = {vr[2].x, vr[2].y, vr[2].z, vr[2].w};
+        const uint32_t W3[4] = {vr[3].x, vr[3].y, vr[3].z, vr[3].w};
+        if constexpr (ELT == 1) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+#pragma unroll
+            for (int sh = 0; sh < 2; ++sh) {
+              const int mt = bx * 8 + 2 * w + sh;
+              // bytes (2sh, 2sh+1) of the word: element pair (d0, d0+1) of m-tile mt
+              const uint32_t X = __byte_perm(W0[w], W1[w], sh ? 0x7362 : 0x5140);  // [k0 d0, k1 d0, k0 d1, k1 d1]
+              const uint32_t Y = __byte_perm(W2[w], W3[w], sh ? 0x7362 : 0x5140);
+              uint32_t a0, a1, a2, a3;
+              if constexpr (KV == kKvE4m3) {
+                a0 = e4m3x2_to_f16x2(X);
+                a1 = e4m3x2_to_f16x2(X >> 16);
+                a2 = e4m3x2_to_f16x2(Y);
+                a3 = e4m3x2_to_f16x2(Y >> 16);
+              } else {
+                a0 = e5m2_bytes_to_f16x2<0, 1>(X);
+                a1 = e5m2_bytes_to_f16x2<2, 3>(X);
+                a2 = e5m2_bytes_to_f16x2<0, 1>(Y);
+                a3 = e5m2_bytes_to_f16x2<2, 3>(Y);
+              }
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) mma_16816(o[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int mt = bx * 4 + w;
+            const uint32_t a0 = __byte_perm(W0[w], W1[w], 0x5410);
+            const uint32_t a1 = __byte_perm(W0[w], W1[w], 0x7632);
+            const uint32_t a2 = __byte_perm(W2[w], W3[w], 0x5410);
+            const uint32_t a3 = __byte_perm(W2[w], W3[w], 0x7632);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_16816(o[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+
+  // ------------------------------------------------------------------ combine the token slices
+  // full row sums of this warp
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) l_run[nt][e] += __shfl_xor_sync(0xffffffffu, l_run[nt][e], off);
+
+  // all consumers are done with the stage ring before it is reused
+  asm volatile("bar.sync 1, %0;" ::"r"(ncw * 32) : "memory");
+
+  float* obuf = reinterpret_cast<float*>(smem);  // [ncw][ROWS_W][D]
+  float* my_o = obuf + static_cast<size_t>(warp) * ROWS_W * D;
+  if (g8 == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        ml_buf[warp * ROWS_W + nt * 8 + 2 * c + e] = make_float2(alive ? m_run[nt][e] : -CUDART_INF_F, l_run[nt][e]);
+  }
+#pragma unroll
+  for (int i = 0; i < MTILES; ++i) {
+    const int d0 = pv_elem(ELT, i, g8);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float* rowp = my_o + (nt * 8 + 2 * c + e) * D;
+        *reinterpret_cast<float2*>(rowp + d0) = make_float2(o[i][nt][e], o[i][nt][2 + e]);
+      }
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(ncw * 32) : "memory");
+
+  // each consumer thread finishes (row, 4 consecutive dims) items
+  const int rows_cta = min(R, p.nrg * ROWS_W);
+  const bool final_out = (nsplit_b == 1);
+  const int items = rows_cta * (D / 4);
+  for (int idx = threadIdx.x; idx < items; idx += ncw * 32) {
+    const int r = idx / (D / 4);
+    const int d = (idx - r * (D / 4)) * 4;
+    const int rgr = r / ROWS_W, rr = r - rgr * ROWS_W;
+    float M = -CUDART_INF_F;
+    for (int t = 0; t < p.nts; ++t) M = fmaxf(M, ml_buf[(rgr * p.nts + t) * ROWS_W + rr].x);
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -CUDART_INF_F) {
+      for (int t = 0; t < p.nts; ++t) {
+        const int wi = rgr * p.nts + t;
+        const float2 ml = ml_buf[wi * ROWS_W + rr];
+        const float w = (ml.x == -CUDART_INF_F) ? 0.f : fast_exp2(ml.x - M);
+        L += w * ml.y;
+        const float4 v = *reinterpret_cast<const float4*>(obuf + (static_cast<size_t>(wi) * ROWS_W + rr) * D + d);
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+      }
+    }
+    const bool has = (M != -CUDART_INF_F) && (L > 0.f);
+    const float inv = has ? vscale / L : 0.f;
+    const int t = r / p.G, j = r - t * p.G;
+    const size_t grow = (static_cast<size_t>(b) * p.T + t) * p.num_q_heads + kvh * p.G + j;
+    // natural-log LSE from base-2 running values
+    const float lse_val = has ? (M + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
+    if (final_out) {
+      __half2 h01 = __floats2half2_rn(acc.x * inv, acc.y * inv);
+      __half2 h23 = __floats2half2_rn(acc.z * inv, acc.w * inv);
+      uint2 packed;
+      packed.x = *reinterpret_cast<uint32_t*>(&h01);
+      packed.y = *reinterpret_cast<uint32_t*>(&h23);
+      *reinterpret_cast<uint2*>(p.out + grow * D + d) = packed;
+      if (d == 0) p.lse[grow] = lse_val;
+    } else {
+      float* dst = p.o_part + (grow * p.num_splits + split) * D + d;
+      *reinterpret_cast<float4*>(dst) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      if (d == 0) p.lse_part[grow * p.num_splits + split] = lse_val;
+    }
+  }
+}
+
+}  // namespace pfkv

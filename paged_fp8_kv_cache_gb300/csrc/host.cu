@@ -1,0 +1,456 @@
+// C ABI of libpfkv.so (declared in include/pfkv.h): argument validation,
+// split-KV planning, TMA descriptor set-up and kernel launches on the
+// caller's stream. Nothing here allocates device memory or synchronises.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+
+#include "../../include/pfkv.h"
+#include "frag_layout.h"
+#include "pfkv_internal.h"
+
+namespace pfkv {
+
+cudaError_t launch_decode_fp16(const DecodeLaunch&, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, dim3,
+                               cudaStream_t);
+cudaError_t launch_decode_e4m3(const DecodeLaunch&, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, dim3,
+                               cudaStream_t);
+cudaError_t launch_decode_e5m2(const DecodeLaunch&, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, dim3,
+                               cudaStream_t);
+int decode_smem_fp16(const DecodeLaunch&, int);
+int decode_smem_e4m3(const DecodeLaunch&, int);
+int decode_smem_e5m2(const DecodeLaunch&, int);
+int decode_ctas_fp16(const DecodeLaunch&, int);
+int decode_ctas_e4m3(const DecodeLaunch&, int);
+int decode_ctas_e5m2(const DecodeLaunch&, int);
+
+__device__ unsigned g_pfkv_err;  // per-device error word (PFKV_DEVERR_* bits)
+
+namespace {
+
+thread_local std::string g_last_error;
+
+pfkv_status fail(pfkv_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+pfkv_status fail(pfkv_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+pfkv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PFKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sm_count[kMaxDevices];
+unsigned* g_err_ptr[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+struct TmKey {
+  const void* ptr;
+  int dev, kv, head_dim, page_size;
+  long long rows;
+  bool operator==(const TmKey& o) const {
+    return ptr == o.ptr && dev == o.dev && kv == o.kv && head_dim == o.head_dim && page_size == o.page_size &&
+           rows == o.rows;
+  }
+};
+struct TmHash {
+  size_t operator()(const TmKey& k) const {
+    size_t h = std::hash<const void*>()(k.ptr);
+    h ^= std::hash<long long>()(k.rows * 1315423911LL + k.head_dim * 31 + k.page_size * 7 + k.kv + k.dev * 101);
+    return h;
+  }
+};
+std::unordered_map<TmKey, CUtensorMap, TmHash> g_tmaps;
+std::unordered_map<long long, int> g_occ;  // (device, kv, D, nt, ncw) -> CTAs per SM
+
+cudaError_t current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return e;
+  if (*dev < 0 || *dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  return cudaSuccess;
+}
+
+cudaError_t sm_count(int dev, int* n) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_sm_count[dev] == 0) {
+    cudaError_t e = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  *n = g_sm_count[dev];
+  return cudaSuccess;
+}
+
+cudaError_t err_word(int dev, unsigned** p) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* a = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&a, g_pfkv_err);
+    if (e != cudaSuccess) return e;
+    g_err_ptr[dev] = static_cast<unsigned*>(a);
+  }
+  *p = g_err_ptr[dev];
+  return cudaSuccess;
+}
+
+pfkv_status get_encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode) return PFKV_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return fail(PFKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return PFKV_OK;
+}
+
+// Tensor map over a cache pool viewed as rows of head_dim elements:
+// [num_blocks * Hkv * page_size rows][head_dim], 128-byte boxes of
+// min(page_size, 64) rows, 128-byte swizzle.
+pfkv_status tensor_map(int dev, const void* pool, int kv, int head_dim, int page_size, long long rows,
+                       CUtensorMap* out) {
+  TmKey key{pool, dev, kv, head_dim, page_size, rows};
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_tmaps.find(key);
+    if (it != g_tmaps.end()) {
+      *out = it->second;
+      return PFKV_OK;
+    }
+  }
+  pfkv_status st = get_encoder();
+  if (st != PFKV_OK) return st;
+  const int elt = kv == kKvFp16 ? 2 : 1;
+  CUtensorMap m;
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(head_dim) * elt};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBoxBytes / elt),
+                       static_cast<cuuint32_t>(page_size < kTileKeys ? page_size : kTileKeys)};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = g_encode(&m, elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+                        const_cast<void*>(pool), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PFKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_tmaps.size() > 256) g_tmaps.clear();
+    g_tmaps[key] = m;
+  }
+  *out = m;
+  return PFKV_OK;
+}
+
+int kv_of(pfkv_kv_dtype d) {
+  return d == PFKV_KV_FP16 ? kKvFp16 : (d == PFKV_KV_FP8_E4M3 ? kKvE4m3 : kKvE5m2);
+}
+
+bool valid_dtype(pfkv_kv_dtype d) {
+  return d == PFKV_KV_FP16 || d == PFKV_KV_FP8_E4M3 || d == PFKV_KV_FP8_E5M2;
+}
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int log2i(int x) {
+  int s = 0;
+  while ((1 << s) < x) ++s;
+  return s;
+}
+
+struct Plan {
+  DecodeLaunch cfg;
+  int nrg, nts, ncw;
+  int splits, split_tokens;
+};
+
+int ctas_per_sm(int dev, const DecodeLaunch& cfg, int ncw) {
+  const long long key = (((static_cast<long long>(dev) * 4 + cfg.kv) * 512 + cfg.head_dim) * 4 + cfg.nt) * 64 + ncw;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end()) return it->second;
+  }
+  int n = cfg.kv == kKvFp16 ? decode_ctas_fp16(cfg, ncw)
+                            : (cfg.kv == kKvE4m3 ? decode_ctas_e4m3(cfg, ncw) : decode_ctas_e5m2(cfg, ncw));
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_occ[key] = n;
+  return n;
+}
+
+// Shape checks shared by plan / workspace / decode.
+pfkv_status check_shape(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_kv_dtype dtype, int max_seq_len,
+                        int num_splits) {
+  if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || max_seq_len < 0 || num_splits < 0)
+    return fail(PFKV_ERR_INVALID_ARG, "negative size (num_seqs=%d Hq=%d Hkv=%d max_seq_len=%d num_splits=%d)",
+                num_seqs, Hq, Hkv, max_seq_len, num_splits);
+  if (Hq % Hkv != 0) return fail(PFKV_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d", Hq, Hkv);
+  if (!valid_dtype(dtype)) return fail(PFKV_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(dtype));
+  if (T < 1 || T > 8) return fail(PFKV_ERR_UNSUPPORTED, "num_q_tokens %d outside 1..8", T);
+  if (D != 128 && D != 256) return fail(PFKV_ERR_UNSUPPORTED, "head_dim %d (supported: 128, 256)", D);
+  if (!is_pow2(P) || P < 16 || P > 2048)
+    return fail(PFKV_ERR_UNSUPPORTED, "page_size %d (supported: powers of two 16..2048)", P);
+  if (T * (Hq / Hkv) > 64)
+    return fail(PFKV_ERR_UNSUPPORTED, "num_q_tokens * group size = %d > 64 rows per KV head", T * (Hq / Hkv));
+  return PFKV_OK;
+}
+
+pfkv_status make_plan(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_kv_dtype dtype, int max_seq_len,
+                      int num_splits_request, Plan* pl) {
+  pfkv_status st = check_shape(num_seqs, T, Hq, Hkv, D, P, dtype, max_seq_len, num_splits_request);
+  if (st != PFKV_OK) return st;
+  const int R = T * (Hq / Hkv);
+  pl->cfg.head_dim = D;
+  pl->cfg.kv = kv_of(dtype);
+  pl->cfg.nt = R <= 8 ? 1 : 2;
+  const int rows_w = 8 * pl->cfg.nt;
+  pl->nrg = (R + rows_w - 1) / rows_w;
+  pl->nts = pl->nrg == 1 ? 4 : 2;
+  pl->ncw = pl->nrg * pl->nts;
+  const int tiles = max_seq_len > 0 ? (max_seq_len + kTileKeys - 1) / kTileKeys : 1;
+  int want;
+  if (num_splits_request > 0) {
+    want = num_splits_request;
+  } else {
+    int dev, sms;
+    cudaError_t e = current_device(&dev);
+    if (e == cudaSuccess) e = sm_count(dev, &sms);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    const int units = num_seqs > 0 ? num_seqs * Hkv : 1;
+    const int target = sms * ctas_per_sm(dev, pl->cfg, pl->ncw);
+    const int base = (target + units - 1) / units;
+    // bound the keys per CTA so ragged batches balance; the bound grows with
+    // the row count because every range costs an fp32 partial per row
+    const int max_keys = R * 256 > 2048 ? R * 256 : 2048;
+    const int need = (max_seq_len + max_keys - 1) / max_keys;
+    const int k = base > 0 ? (need + base - 1) / base : 1;
+    want = base * (k > 1 ? k : 1);
+  }
+  if (want < 1) want = 1;
+  if (want > tiles) want = tiles;
+  const int tiles_per_split = (tiles + want - 1) / want;
+  pl->split_tokens = tiles_per_split * kTileKeys;
+  pl->splits = (tiles + tiles_per_split - 1) / tiles_per_split;
+  return PFKV_OK;
+}
+
+size_t workspace_for(const Plan& pl, int num_seqs, int T, int Hq, int D) {
+  if (pl.splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(num_seqs) * T * Hq;
+  const size_t o = rows * pl.splits * D * sizeof(float);
+  const size_t l = rows * pl.splits * sizeof(float);
+  return o + l;
+}
+
+}  // namespace
+}  // namespace pfkv
+
+using namespace pfkv;
+
+extern "C" {
+
+const char* pfkv_status_string(pfkv_status s) {
+  switch (s) {
+    case PFKV_OK: return "PFKV_OK";
+    case PFKV_ERR_INVALID_ARG: return "PFKV_ERR_INVALID_ARG";
+    case PFKV_ERR_UNSUPPORTED: return "PFKV_ERR_UNSUPPORTED";
+    case PFKV_ERR_WORKSPACE: return "PFKV_ERR_WORKSPACE";
+    case PFKV_ERR_CUDA: return "PFKV_ERR_CUDA";
+    case PFKV_ERR_DEVICE_CHECK: return "PFKV_ERR_DEVICE_CHECK";
+  }
+  return "PFKV_UNKNOWN_STATUS";
+}
+
+const char* pfkv_last_error(void) { return g_last_error.c_str(); }
+
+uint32_t pfkv_capabilities(void) {
+  return PFKV_CAP_KV_FP16 | PFKV_CAP_KV_FP8_E4M3 | PFKV_CAP_KV_FP8_E5M2 | PFKV_CAP_HEAD_DIM_128 |
+         PFKV_CAP_HEAD_DIM_256 | PFKV_CAP_PAGE_16 | PFKV_CAP_PAGE_2048 | PFKV_CAP_PAGE_POW2_ANY |
+         PFKV_CAP_Q_TOKENS_1_8 | PFKV_CAP_SPLIT_KV;
+}
+
+pfkv_status pfkv_device_errors(uint32_t* flags, int clear) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  unsigned v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_pfkv_err, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  if (clear) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_pfkv_err, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+  }
+  if (flags) *flags = v;
+  return v ? fail(PFKV_ERR_DEVICE_CHECK, "device error word 0x%x", v) : PFKV_OK;
+}
+
+pfkv_status pfkv_kv_cache_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                                 const int64_t* slot_mapping, int n_tok, int num_kv_heads, int head_dim,
+                                 int page_size, int num_blocks, pfkv_kv_dtype dtype, const float* k_scale,
+                                 const float* v_scale, pfkv_stream_t stream) {
+  if (n_tok < 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0 || num_blocks <= 0)
+    return fail(PFKV_ERR_INVALID_ARG, "bad size (n_tok=%d Hkv=%d D=%d P=%d num_blocks=%d)", n_tok, num_kv_heads,
+                head_dim, page_size, num_blocks);
+  if (!valid_dtype(dtype)) return fail(PFKV_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(dtype));
+  if (head_dim % 8 != 0 || head_dim > 1024)
+    return fail(PFKV_ERR_UNSUPPORTED, "head_dim %d (must be a multiple of 8, at most 1024)", head_dim);
+  if (n_tok == 0) return PFKV_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping)
+    return fail(PFKV_ERR_INVALID_ARG, "null pointer");
+  if (dtype != PFKV_KV_FP16 && (!k_scale || !v_scale)) return fail(PFKV_ERR_INVALID_ARG, "null scale pointer");
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
+       reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15)
+    return fail(PFKV_ERR_INVALID_ARG, "K/V and cache pointers must be 16-byte aligned");
+  int dev;
+  unsigned* err;
+  cudaError_t e = current_device(&dev);
+  if (e == cudaSuccess) e = err_word(dev, &err);
+  if (e != cudaSuccess) return cuda_fail(e, "device set-up");
+  e = launch_append(static_cast<const __half*>(k_new), static_cast<const __half*>(v_new), k_cache, v_cache,
+                    slot_mapping, n_tok, num_kv_heads, head_dim, page_size, num_blocks, kv_of(dtype), k_scale, v_scale,
+                    err, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PFKV_OK : cuda_fail(e, "append launch");
+}
+
+pfkv_status pfkv_decode_plan(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                             int page_size, pfkv_kv_dtype dtype, int max_seq_len, int num_splits_request,
+                             int* num_splits, int* split_tokens) {
+  Plan pl;
+  pfkv_status st = make_plan(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype,
+                             max_seq_len, num_splits_request, &pl);
+  if (st != PFKV_OK) return st;
+  if (num_splits) *num_splits = pl.splits;
+  if (split_tokens) *split_tokens = pl.split_tokens;
+  return PFKV_OK;
+}
+
+size_t pfkv_decode_workspace_bytes(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int page_size, pfkv_kv_dtype dtype, int max_seq_len, int num_splits_request) {
+  Plan pl;
+  if (make_plan(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype, max_seq_len,
+                num_splits_request, &pl) != PFKV_OK)
+    return 0;
+  return workspace_for(pl, num_seqs, num_q_tokens, num_q_heads, head_dim);
+}
+
+pfkv_status pfkv_paged_attention_decode(void* out, float* lse, const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                                        int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int page_size, int num_blocks, pfkv_kv_dtype dtype,
+                                        const float* k_scale, const float* v_scale, float softmax_scale,
+                                        int max_seq_len, int num_splits, void* workspace, size_t workspace_bytes,
+                                        pfkv_stream_t stream) {
+  Plan pl;
+  pfkv_status st = make_plan(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype,
+                             max_seq_len, num_splits, &pl);
+  if (st != PFKV_OK) return st;
+  if (num_seqs == 0) return PFKV_OK;
+  if (!out || !lse || !q || !k_cache || !v_cache || !block_table || !seq_lens)
+    return fail(PFKV_ERR_INVALID_ARG, "null pointer");
+  if (dtype != PFKV_KV_FP16 && (!k_scale || !v_scale)) return fail(PFKV_ERR_INVALID_ARG, "null scale pointer");
+  if (num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return fail(PFKV_ERR_INVALID_ARG, "num_blocks=%d max_blocks_per_seq=%d", num_blocks, max_blocks_per_seq);
+  const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * page_size;
+  if (rows > 0x7fffffffLL) return fail(PFKV_ERR_UNSUPPORTED, "cache pool of %lld rows exceeds 2^31", rows);
+  if (static_cast<long long>(max_blocks_per_seq) * page_size > 0x7fffffffLL)
+    return fail(PFKV_ERR_UNSUPPORTED, "max_blocks_per_seq * page_size exceeds 2^31");
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15)
+    return fail(PFKV_ERR_INVALID_ARG, "cache pools must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 7)
+    return fail(PFKV_ERR_INVALID_ARG, "q and out must be 8-byte aligned");
+  if (reinterpret_cast<uintptr_t>(lse) & 3) return fail(PFKV_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  const size_t need = workspace_for(pl, num_seqs, num_q_tokens, num_q_heads, head_dim);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need)
+      return fail(PFKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) & 15)
+      return fail(PFKV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  }
+  int dev;
+  unsigned* err;
+  cudaError_t e = current_device(&dev);
+  if (e == cudaSuccess) e = err_word(dev, &err);
+  if (e != cudaSuccess) return cuda_fail(e, "device set-up");
+
+  CUtensorMap tmk, tmv;
+  const int kv = kv_of(dtype);
+  st = tensor_map(dev, k_cache, kv, head_dim, page_size, rows, &tmk);
+  if (st != PFKV_OK) return st;
+  st = tensor_map(dev, v_cache, kv, head_dim, page_size, rows, &tmv);
+  if (st != PFKV_OK) return st;
+
+  DecodeParams p;
+  p.q = static_cast<const __half*>(q);
+  p.out = static_cast<__half*>(out);
+  p.lse = lse;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  const size_t nrows = static_cast<size_t>(num_seqs) * num_q_tokens * num_q_heads;
+  p.o_part = need ? static_cast<float*>(workspace) : nullptr;
+  p.lse_part = need ? static_cast<float*>(workspace) + nrows * pl.splits * head_dim : nullptr;
+  p.err = err;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.T = num_q_tokens;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.G = num_q_heads / num_kv_heads;
+  p.page_size = page_size;
+  p.page_shift = log2i(page_size);
+  p.num_blocks = num_blocks;
+  p.max_seq_len = max_seq_len;
+  p.split_tokens = pl.split_tokens;
+  p.num_splits = pl.splits;
+  p.nrg = pl.nrg;
+  p.nts = pl.nts;
+  p.softmax_scale = softmax_scale;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  dim3 grid(pl.splits, num_kv_heads, num_seqs);
+  e = kv == kKvFp16 ? launch_decode_fp16(pl.cfg, tmk, tmv, p, grid, s)
+                    : (kv == kKvE4m3 ? launch_decode_e4m3(pl.cfg, tmk, tmv, p, grid, s)
+                                     : launch_decode_e5m2(pl.cfg, tmk, tmv, p, grid, s));
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (pl.splits > 1) {
+    const long long cap_ll = static_cast<long long>(max_blocks_per_seq) * page_size;
+    const int cap = static_cast<int>(cap_ll < max_seq_len ? cap_ll : max_seq_len);
+    e = launch_lse_merge(p.out, lse, p.o_part, p.lse_part, static_cast<int>(nrows), pl.splits, head_dim, seq_lens,
+                         num_q_tokens * num_q_heads, pl.split_tokens, max_seq_len, cap, s);
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  }
+  return PFKV_OK;
+}
+
+pfkv_status pfkv_lse_merge(void* out, float* lse, const float* o_parts, const float* lse_parts, int rows,
+                           int num_parts, int head_dim, pfkv_stream_t stream) {
+  if (rows < 0 || num_parts <= 0 || head_dim <= 0)
+    return fail(PFKV_ERR_INVALID_ARG, "bad size (rows=%d parts=%d D=%d)", rows, num_parts, head_dim);
+  if (head_dim % 4 != 0 || head_dim > 1024)
+    return fail(PFKV_ERR_UNSUPPORTED, "head_dim %d (multiple of 4, at most 1024)", head_dim);
+  if (rows == 0) return PFKV_OK;
+  if (!out || !o_parts || !lse_parts) return fail(PFKV_ERR_INVALID_ARG, "null pointer");
+  if ((reinterpret_cast<uintptr_t>(o_parts) & 15) || (reinterpret_cast<uintptr_t>(out) & 7))
+    return fail(PFKV_ERR_INVALID_ARG, "o_parts must be 16-byte and out 8-byte aligned");
+  if (static_cast<long long>(rows) * num_parts * head_dim > (1LL << 40))
+    return fail(PFKV_ERR_INVALID_ARG, "too large");
+  cudaError_t e = launch_lse_merge(static_cast<__half*>(out), lse, o_parts, lse_parts, rows, num_parts, head_dim,
+                                   nullptr, 1, 1, 0, 0, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PFKV_OK : cuda_fail(e, "merge launch");
+}
+
+}  // extern "C"

@@ -11,3 +11,11 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: full-size workload (minutes)")
+
+
+@pytest.fixture(scope="session")
+def pflib():
+    """The built libpfkv.so (built in-tree first if any source is newer)."""
+    from paged_fp8_kv_cache_gb300 import binding, build
+    build.build()
+    return binding.load()

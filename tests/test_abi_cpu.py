@@ -1,0 +1,112 @@
+"""The C-ABI library builds, loads and exports what include/pfkv.h declares;
+host-side validation and split planning work without a GPU (CPU only)."""
+
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+from paged_fp8_kv_cache_gb300 import binding as pf
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pfkv.h")
+CSRC = os.path.join(ROOT, "paged_fp8_kv_cache_gb300", "csrc")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pfkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_binding_lists_every_declared_function():
+    assert sorted(pf.EXPORTS) == declared_functions()
+
+
+def test_library_exports_every_declared_symbol(pflib):
+    lib = ctypes.CDLL(pf.LIB_PATH)
+    missing = [f for f in declared_functions() if not hasattr(lib, f)]
+    assert not missing, missing
+
+
+def test_exports_nothing_else(pflib):
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", pf.LIB_PATH], capture_output=True, text=True).stdout
+    pfkv = sorted({ln.split()[-1] for ln in out.splitlines() if " T pfkv_" in ln})
+    assert pfkv == declared_functions()
+
+
+def test_status_strings_and_capabilities(pflib):
+    for st, name in [(0, "PFKV_OK"), (1, "PFKV_ERR_INVALID_ARG"), (2, "PFKV_ERR_UNSUPPORTED"),
+                     (3, "PFKV_ERR_WORKSPACE"), (4, "PFKV_ERR_CUDA"), (5, "PFKV_ERR_DEVICE_CHECK")]:
+        assert pf.pfkv_status_string(st) == name
+    caps = pf.pfkv_capabilities()
+    for bit in (0x1, 0x2, 0x4, 0x10, 0x20, 0x100, 0x200, 0x1000, 0x2000):
+        assert caps & bit
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(T=9), pf.PFKV_ERR_UNSUPPORTED),
+    (dict(D=64), pf.PFKV_ERR_UNSUPPORTED),
+    (dict(P=24), pf.PFKV_ERR_UNSUPPORTED),
+    (dict(P=4096), pf.PFKV_ERR_UNSUPPORTED),
+    (dict(Hq=30), pf.PFKV_ERR_INVALID_ARG),
+    (dict(T=8, Hq=72, Hkv=8), pf.PFKV_ERR_UNSUPPORTED),  # 8 tokens x group 9 = 72 rows > 64
+    (dict(B=-1), pf.PFKV_ERR_INVALID_ARG),
+    (dict(kv=7), pf.PFKV_ERR_INVALID_ARG),
+])
+def test_plan_rejects_bad_shapes(pflib, args, status):
+    a = dict(B=2, T=1, Hq=32, Hkv=8, D=128, P=16, kv=1, msl=4096, S=4)
+    a.update(args)
+    with pytest.raises(pf.PfkvError) as ei:
+        pf.pfkv_decode_plan(a["B"], a["T"], a["Hq"], a["Hkv"], a["D"], a["P"], a["kv"], a["msl"], a["S"])
+    assert ei.value.status == status
+
+
+@pytest.mark.parametrize("msl,req,exp", [
+    (4096, 1, (1, 4096)), (4096, 2, (2, 2048)), (5000, 7, (7, 768)), (100, 7, (2, 64)),
+    (0, 3, (1, 64)), (262144, 38, (38, 6912)), (1, 1, (1, 64)),
+])
+def test_split_plan_with_explicit_count(pflib, msl, req, exp):
+    # explicit counts need no device query: ranges are whole 64-key tiles
+    assert pf.pfkv_decode_plan(4, 1, 32, 8, 128, 16, "e4m3", msl, req) == exp
+    S, C = exp
+    assert S * C >= msl and (S - 1) * C < max(msl, 1)
+
+
+def test_decode_validation_before_any_launch(pflib):
+    lib = pf.load()
+    # null pointers with a valid shape and an explicit split count: rejected on the host
+    st = lib.pfkv_paged_attention_decode(None, None, None, None, None, None, 4, None, 2, 1, 32, 8, 128, 16, 64,
+                                         1, None, None, ctypes.c_float(0.1), 64, 1, None, 0, None)
+    assert st == pf.PFKV_ERR_INVALID_ARG
+    # zero sequences is a no-op
+    st = lib.pfkv_paged_attention_decode(None, None, None, None, None, None, 4, None, 0, 1, 32, 8, 128, 16, 64,
+                                         1, None, None, ctypes.c_float(0.1), 64, 1, None, 0, None)
+    assert st == pf.PFKV_OK
+    # append: zero tokens is a no-op; bad head_dim is unsupported; null pointers invalid
+    assert lib.pfkv_kv_cache_append(None, None, None, None, None, 0, 8, 128, 16, 10, 1, None, None, None) == 0
+    assert lib.pfkv_kv_cache_append(None, None, None, None, None, 4, 8, 100, 16, 10, 1, None, None, None) == \
+        pf.PFKV_ERR_UNSUPPORTED
+    assert lib.pfkv_kv_cache_append(None, None, None, None, None, 4, 8, 128, 16, 10, 1, None, None, None) == \
+        pf.PFKV_ERR_INVALID_ARG
+    assert "null" in pf.pfkv_last_error()
+    # merge: bad sizes
+    assert lib.pfkv_lse_merge(None, None, None, None, 4, 0, 128, None) == pf.PFKV_ERR_INVALID_ARG
+    assert lib.pfkv_lse_merge(None, None, None, None, 0, 3, 128, None) == pf.PFKV_OK
+
+
+def test_fragment_layout_checker(tmp_path):
+    gxx = shutil.which("g++") or shutil.which("c++")
+    if gxx is None:
+        pytest.skip("no host C++ compiler")
+    exe = tmp_path / "layout_check"
+    subprocess.run([gxx, "-std=c++17", "-O1", os.path.join(CSRC, "layout_check.cpp"), "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    assert "layout ok" in r.stdout
