@@ -150,6 +150,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": n}
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise max of per-rank timings (every rank gets the result)."""
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if dist is not None and dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def rank_seed(spec, rank: int) -> int:
+    """Each rank decodes its own batch of the workload (weak scaling); rank 0 the canonical one."""
+    return spec.seed + 1000 * rank
+
+
+def aggregate_gbs(bytes_per_rank_step: int, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job effective GB/s: bytes every rank processed / the slowest rank's time."""
+    return bytes_per_rank_step * world * steps / (max_ms * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 class DeviceWorkload:
@@ -277,7 +296,7 @@ def run_gpu(args):
 
     wid = args.workload
     spec = workloads.CONFIGS[wid]
-    case = workloads.make_case(spec, seed=spec.seed + 1000 * rank)
+    case = workloads.make_case(spec, seed=rank_seed(spec, rank))
     dw = DeviceWorkload(case, torch, pf)
     flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     nbytes = algorithmic_bytes(case, dw.has_append)
@@ -295,14 +314,11 @@ def run_gpu(args):
     if pf.pfkv_device_errors(clear=True):
         raise RuntimeError("device error word set during the benchmark")
 
-    t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device="cuda")
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dist, "cuda")
     if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
         dist.barrier()
-    total_ms, e2e_ms = float(t[0]), float(t[1])
-    all_bytes = nbytes * world  # every rank runs one batch of the workload per step (weak scaling)
-    value = all_bytes * args.steps / (total_ms * 1e-3) / 1e9
-    e2e_val = all_bytes * args.steps / (e2e_ms * 1e-3) / 1e9
+    value = aggregate_gbs(nbytes, world, args.steps, total_ms)
+    e2e_val = aggregate_gbs(nbytes, world, args.steps, e2e_ms)
 
     if rank != 0:
         if world > 1:
@@ -412,39 +428,57 @@ def _oracle_unit(u):
     return int(case.seq_lens[b]) * s.head_dim * elt * 2
 
 
-def oracle_sample(wid, budget_s=20.0, seed=None):
-    """Time the oracle on the host cores over a bounded sample of (sequence, KV head) units."""
-    import multiprocessing as mp
-    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ[var] = "1"
-    cores = len(os.sched_getaffinity(0))
-    spec = workloads.CONFIGS[wid]
-    seed = spec.seed if seed is None else seed
-    ctx = mp.get_context("spawn")
-    with ctx.Pool(cores, initializer=_oracle_worker_init, initargs=(wid, seed)) as pool:
-        pool.map(abs, range(cores))  # wait until every worker has its inputs
-        case = workloads.make_case(spec, seed=seed)
-        units = [(b, h) for b in range(case.B) for h in range(spec.num_kv_heads)]
+class OraclePool:
+    """The CPU oracle on a spawned process pool (one single-threaded worker per core)."""
+
+    def __init__(self, wid, seed=None):
+        import multiprocessing as mp
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = "1"
+        self.cores = len(os.sched_getaffinity(0))
+        self.spec = workloads.CONFIGS[wid]
+        seed = self.spec.seed if seed is None else seed
+        self.pool = mp.get_context("spawn").Pool(self.cores, initializer=_oracle_worker_init, initargs=(wid, seed))
+        self.pool.map(abs, range(self.cores))  # wait until every worker holds its inputs
+        self.case = workloads.make_case(self.spec, seed=seed)
+        units = [(b, h) for b in range(self.case.B) for h in range(self.spec.num_kv_heads)]
         rng = np.random.default_rng(0)
-        order = [units[i] for i in rng.permutation(len(units))]
-        # grow the sample until it takes about budget_s of wall time (or covers every unit)
-        done, kv_bytes, t_total, n = 0, 0, 0.0, cores
-        while done < len(order):
-            batch = order[done:done + n]
+        self.order = [units[i] for i in rng.permutation(len(units))]
+        self.next = 0
+        self.step_bytes = algorithmic_bytes(self.case, self.case.slot_new.size > 0)
+
+    def run(self, budget_s):
+        """Evaluate (sequence, KV head) units, cycling through the workload, for about budget_s."""
+        kv_bytes, t_total, evals = 0, 0.0, 0
+        n = self.cores
+        while t_total < budget_s:
+            batch = [self.order[(self.next + i) % len(self.order)] for i in range(n)]
+            self.next = (self.next + n) % len(self.order)
             t0 = time.perf_counter()
-            kv_bytes += sum(pool.map(_oracle_unit, batch, chunksize=1))
+            kv_bytes += sum(self.pool.map(_oracle_unit, batch, chunksize=1))
             t_total += time.perf_counter() - t0
-            done += len(batch)
-            if t_total >= budget_s:
-                break
-            n = min(len(order) - done, max(cores, n * 2))
-    frac = kv_bytes / max(1, case.kv_bytes())
-    total_bytes = algorithmic_bytes(case, case.slot_new.size > 0)
-    sample_bytes = total_bytes * frac
-    return {"value": round(sample_bytes / t_total / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done} of {len(order)} (sequence, KV head) units of '{spec.name}' "
-                      f"({100 * frac:.1f}% of the step's KV bytes), {t_total:.1f} s wall on {cores} processes",
-            "seconds": round(t_total, 2)}
+            evals += n
+            if t_total < budget_s / 8:
+                n = min(n * 2, 64 * self.cores)
+        frac = kv_bytes / max(1, self.case.kv_bytes())  # in units of whole steps
+        return {"value": round(self.step_bytes * frac / t_total / 1e9, 4), "unit": "GB/s", "cores": self.cores,
+                "kind": "oracle",
+                "sample": f"{evals} (sequence, KV head) unit evaluations cycling over the {len(self.order)} units of "
+                          f"'{self.spec.name}' (= {frac:.3g} steps of KV bytes) in {t_total:.2f} s wall on "
+                          f"{self.cores} single-threaded processes",
+                "seconds": round(t_total, 3)}
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def oracle_sample(wid, budget_s=15.0):
+    op = OraclePool(wid)
+    try:
+        return op.run(budget_s)
+    finally:
+        op.close()
 
 
 def run_reference(args):
@@ -454,12 +488,16 @@ def run_reference(args):
     spec = workloads.CONFIGS[args.workload]
     vals = []
     info = None
-    per = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
-    for i in range(args.warmup + args.steps):
-        r = oracle_sample(args.workload, budget_s=per)
-        if i >= args.warmup:
-            vals.append(r["value"])
-            info = r
+    per = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    op = OraclePool(args.workload)
+    try:
+        for i in range(args.warmup + args.steps):
+            r = op.run(per)
+            if i >= args.warmup:
+                vals.append(r["value"])
+                info = r
+    finally:
+        op.close()
     v = statistics.median(vals) if vals else 0.0
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
