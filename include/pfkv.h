@@ -199,6 +199,40 @@ PFKV_API pfkv_status pfkv_paged_attention_decode(void* out, float* lse, const vo
                                         pfkv_stream_t stream);
 
 /*
+ * pfkv_paged_attention_decode_static_scratch -- pfkv_paged_attention_decode
+ * for callers that cannot allocate device memory. (An addition of this
+ * library: the pages have no counterpart.)
+ *
+ * Who needs it: code that runs inside another engine's memory pool, which
+ * has already reserved nearly all device memory (typically for its own KV
+ * cache) so that a cudaMalloc would fail, or a latency-critical serving loop
+ * in which cudaMalloc / cudaFree would implicitly synchronise the device.
+ *
+ * Same arguments and results as pfkv_paged_attention_decode, without the
+ * workspace: the split partials go to a fixed 32 MiB array compiled into the
+ * library's device image (every GPU that loads the library holds it until
+ * the process exits). Nothing is allocated or freed, by this call or by
+ * anything it calls.
+ *  - Size limit: if pfkv_decode_workspace_bytes() for these arguments exceeds
+ *    32 MiB (33554432 bytes) the call returns PFKV_ERR_WORKSPACE and enqueues
+ *    nothing. The workloads of this library need at most about 16 MB.
+ *  - Set-up: the first call on each device looks up the array's device
+ *    address (cudaGetSymbolAddress, with that device current) and caches it;
+ *    make that first call before any stream capture.
+ *  - Sharing: every call on a device uses the same array, and it keeps the
+ *    last call's contents (nothing in it needs to start at zero). Calls whose
+ *    work overlaps on the GPU (other streams, or another thread's calls)
+ *    race on it: order them on one stream or synchronise between them.
+ */
+PFKV_API pfkv_status pfkv_paged_attention_decode_static_scratch(
+    void* out, float* lse, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+    int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+    int page_size, int num_blocks, pfkv_kv_dtype dtype, const float* k_scale,
+    const float* v_scale, float softmax_scale, int max_seq_len, int num_splits,
+    pfkv_stream_t stream);
+
+/*
  * pfkv_lse_merge -- combine per-range partial attention results into the
  * final output (the merge step of the split long-context route of [R2]
  * "Flash-V100 long-context improvements"). For each row r:

@@ -39,6 +39,7 @@ EXPORTS = [
     "pfkv_decode_plan",
     "pfkv_decode_workspace_bytes",
     "pfkv_paged_attention_decode",
+    "pfkv_paged_attention_decode_static_scratch",
     "pfkv_lse_merge",
     "pfkv_device_errors",
     "pfkv_capabilities",
@@ -81,6 +82,10 @@ def load(path: str | None = None):
     lib.pfkv_paged_attention_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32,
                                                 i32, vp, vp, ctypes.c_float, i32, i32, vp, ctypes.c_size_t, vp]
     lib.pfkv_paged_attention_decode.restype = i32
+    lib.pfkv_paged_attention_decode_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                                               i32, i32, i32, i32, vp, vp, ctypes.c_float, i32,
+                                                               i32, vp]
+    lib.pfkv_paged_attention_decode_static_scratch.restype = i32
     lib.pfkv_lse_merge.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
     lib.pfkv_lse_merge.restype = i32
     lib.pfkv_device_errors.argtypes = [u32p, i32]
@@ -153,6 +158,19 @@ def pfkv_paged_attention_decode(out, lse, q, k_cache, v_cache, block_table, seq_
         _ptr(seq_lens), num_seqs, num_q_tokens, hq, num_kv_heads, d, page_size, k_cache.shape[0], _kv(kv_dtype),
         _ptr(k_scale), _ptr(v_scale), float(softmax_scale), max_seq_len, num_splits, _ptr(workspace), ws_bytes,
         _stream(stream)))
+
+
+def pfkv_paged_attention_decode_static_scratch(out, lse, q, k_cache, v_cache, block_table, seq_lens, num_q_tokens,
+                                               num_kv_heads, page_size, kv_dtype, k_scale, v_scale, softmax_scale,
+                                               max_seq_len, num_splits=0, stream=None):
+    """Decode with the library's built-in split scratch (for callers that cannot allocate device memory)."""
+    lib = load()
+    num_seqs = seq_lens.shape[0]
+    hq, d = q.shape[1], q.shape[2]
+    _check(lib.pfkv_paged_attention_decode_static_scratch(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), num_seqs, num_q_tokens, hq, num_kv_heads, d, page_size, k_cache.shape[0], _kv(kv_dtype),
+        _ptr(k_scale), _ptr(v_scale), float(softmax_scale), max_seq_len, num_splits, _stream(stream)))
 
 
 def pfkv_lse_merge(out, lse, o_parts, lse_parts, stream=None):

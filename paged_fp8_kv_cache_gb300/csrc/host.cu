@@ -454,3 +454,60 @@ pfkv_status pfkv_lse_merge(void* out, float* lse, const float* o_parts, const fl
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode without caller-provided scratch.
+//
+// Some callers cannot allocate device memory: for example a plugin running
+// inside another engine whose memory pool reserved nearly all of the GPU for
+// its KV cache up front (a fresh cudaMalloc would fail), or a latency-critical
+// serving loop where cudaMalloc/cudaFree would implicitly synchronise the
+// device. For them the split partials live in a fixed array that is part of
+// this library's device image: every GPU that loads the library holds
+// kPfkvStaticScratchBytes of it until the process exits.
+namespace {
+
+constexpr size_t kPfkvStaticScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_pfkv_static_scratch[kPfkvStaticScratchBytes];
+void* g_static_scratch_ptr[kMaxDevices];
+
+// Device address of the array on the current device. In host code the
+// array's name is only a host-side stand-in, never a device address: it is
+// looked up once per device (with that device current) and cached.
+pfkv_status static_scratch_address(void** out) {
+  int dev;
+  cudaError_t e = current_device(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_static_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_pfkv_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_static_scratch_ptr[dev] = p;
+  }
+  *out = g_static_scratch_ptr[dev];
+  return PFKV_OK;
+}
+
+}  // namespace
+
+extern "C" pfkv_status pfkv_paged_attention_decode_static_scratch(
+    void* out, float* lse, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+    int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs, int num_q_tokens, int num_q_heads,
+    int num_kv_heads, int head_dim, int page_size, int num_blocks, pfkv_kv_dtype dtype, const float* k_scale,
+    const float* v_scale, float softmax_scale, int max_seq_len, int num_splits, pfkv_stream_t stream) {
+  const size_t need = pfkv_decode_workspace_bytes(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim,
+                                                  page_size, dtype, max_seq_len, num_splits);
+  if (need > kPfkvStaticScratchBytes)
+    return fail(PFKV_ERR_WORKSPACE,
+                "this call needs %zu bytes of split scratch; the built-in array holds %zu (use fewer splits, "
+                "fewer sequences or pfkv_paged_attention_decode with your own workspace)",
+                need, kPfkvStaticScratchBytes);
+  void* scratch = nullptr;
+  pfkv_status st = static_scratch_address(&scratch);
+  if (st != PFKV_OK) return st;
+  return pfkv_paged_attention_decode(out, lse, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
+                                     num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size,
+                                     num_blocks, dtype, k_scale, v_scale, softmax_scale, max_seq_len, num_splits,
+                                     scratch, kPfkvStaticScratchBytes, stream);
+}
