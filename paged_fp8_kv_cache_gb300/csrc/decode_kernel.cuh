@@ -44,7 +44,7 @@ struct DecodeShape {
   static constexpr int NBOX = ROWB / kBoxBytes;
   static constexpr int KV_STAGE = NBOX * kSubTileBytes;  // K (or V) bytes of one stage
   static constexpr int STAGE = 2 * KV_STAGE;
-  static constexpr int NS = STAGE <= 32768 ? 4 : 2;      // pipeline depth
+  static constexpr int NS = STAGE <= 16384 ? 4 : (STAGE <= 32768 ? 3 : 2);  // pipeline depth
   static constexpr int KSTEPS = D / 16;
   static constexpr int MTILES = D / 16;                  // PV m-tiles over the head dim
 };
@@ -60,7 +60,7 @@ constexpr int decode_smem_bytes(int ncw) {
 }
 
 template <int D, int KV, int NT>
-__global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
+__global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeParams p) {
   using S = DecodeShape<D, KV>;
@@ -106,64 +106,94 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
 
   // ------------------------------------------------------------------ producer
   if (warp == ncw) {
-    if (lane == 0 && ntiles > 0) {
-      prefetch_tensormap(&tmk);
-      prefetch_tensormap(&tmv);
+    // The whole warp walks the tiles; its 32 lanes fetch 32 consecutive page
+    // ids of the range at a time (one coalesced load instead of a chain of
+    // dependent ones) and lane 0 issues the copies, reading ids by shuffle.
+    if (ntiles > 0) {
+      if (lane == 0) {
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+      }
       const int P = p.page_size;
       const int* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks;
+      const int page_last = (t1 - 1) >> p.page_shift;
+      int chunk_base = -(1 << 30);  // first page index held by the lanes' ids (none yet)
+      int my_id = 0;
+      auto page_id = [&](int pidx) -> int {
+        if (pidx < chunk_base || pidx >= chunk_base + 32) {
+          chunk_base = pidx;
+          const int mine = chunk_base + lane;
+          my_id = 0;
+          if (mine <= page_last) {
+            my_id = bt[mine];
+            if (static_cast<unsigned>(my_id) >= static_cast<unsigned>(p.num_blocks)) {
+              atomicOr(p.err, kDevErrBlockId);
+              my_id = 0;
+            }
+          }
+        }
+        return __shfl_sync(0xffffffffu, my_id, pidx - chunk_base);
+      };
       bool ok = true;
       for (int it = 0; it < ntiles && ok; ++it) {
         const int s = it % NS;
-        if (it >= NS && !mbar_wait(&empty[s], ((it / NS) - 1) & 1)) {
-          atomicOr(p.err, kDevErrTimeout);
-          ok = false;
-          break;
+        if (it >= NS) {
+          bool got = true;
+          if (lane == 0) got = mbar_wait(&empty[s], ((it / NS) - 1) & 1);
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) {
+            if (lane == 0) atomicOr(p.err, kDevErrTimeout);
+            ok = false;
+            break;
+          }
         }
         unsigned char* kdst = smem + s * S::STAGE;
         unsigned char* vdst = kdst + S::KV_STAGE;
         const int tile_start = t0 + it * kTileKeys;
         if (P >= kTileKeys) {
-          int blk = bt[tile_start >> p.page_shift];
-          if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
-            atomicOr(p.err, kDevErrBlockId);
-            blk = 0;
-          }
+          const int blk = page_id(tile_start >> p.page_shift);
           const int row = (blk * p.num_kv_heads + kvh) * P + (tile_start & (P - 1));
-          mbar_arrive_expect_tx(&full[s], 2 * S::KV_STAGE);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full[s], 2 * S::KV_STAGE);
 #pragma unroll
-          for (int bx = 0; bx < NBOX; ++bx) {
-            tma_load_2d(kdst + bx * kSubTileBytes, &tmk, &full[s], bx * (kBoxBytes / ELT), row);
-            tma_load_2d(vdst + bx * kSubTileBytes, &tmv, &full[s], bx * (kBoxBytes / ELT), row);
+            for (int bx = 0; bx < NBOX; ++bx) {
+              tma_load_2d(kdst + bx * kSubTileBytes, &tmk, &full[s], bx * (kBoxBytes / ELT), row);
+              tma_load_2d(vdst + bx * kSubTileBytes, &tmv, &full[s], bx * (kBoxBytes / ELT), row);
+            }
           }
         } else {
           const int valid = min(kTileKeys, t1 - tile_start);
           const int npages = (valid + P - 1) >> p.page_shift;
-          mbar_arrive_expect_tx(&full[s], 2 * NBOX * npages * P * kBoxBytes);
           const int pfirst = tile_start >> p.page_shift;
+          if (lane == 0) mbar_arrive_expect_tx(&full[s], 2 * NBOX * npages * P * kBoxBytes);
           for (int pg = 0; pg < npages; ++pg) {
-            int blk = bt[pfirst + pg];
-            if (static_cast<unsigned>(blk) >= static_cast<unsigned>(p.num_blocks)) {
-              atomicOr(p.err, kDevErrBlockId);
-              blk = 0;
-            }
+            const int blk = page_id(pfirst + pg);
             const int row = (blk * p.num_kv_heads + kvh) * P;
+            if (lane == 0) {
 #pragma unroll
-            for (int bx = 0; bx < NBOX; ++bx) {
-              tma_load_2d(kdst + bx * kSubTileBytes + pg * P * kBoxBytes, &tmk, &full[s], bx * (kBoxBytes / ELT), row);
-              tma_load_2d(vdst + bx * kSubTileBytes + pg * P * kBoxBytes, &tmv, &full[s], bx * (kBoxBytes / ELT), row);
+              for (int bx = 0; bx < NBOX; ++bx) {
+                tma_load_2d(kdst + bx * kSubTileBytes + pg * P * kBoxBytes, &tmk, &full[s], bx * (kBoxBytes / ELT),
+                            row);
+                tma_load_2d(vdst + bx * kSubTileBytes + pg * P * kBoxBytes, &tmv, &full[s], bx * (kBoxBytes / ELT),
+                            row);
+              }
             }
           }
         }
       }
       // do not leave while copies may still land in this CTA's shared memory
-      const int first_pending = max(0, ntiles - NS);
-      for (int it = first_pending; it < ntiles; ++it) {
-        if (!mbar_wait(&full[it % NS], (it / NS) & 1)) {
-          atomicOr(p.err, kDevErrTimeout);
-          break;
+      if (lane == 0) {
+        const int first_pending = max(0, ntiles - NS);
+        for (int it = first_pending; it < ntiles; ++it) {
+          if (!mbar_wait(&full[it % NS], (it / NS) & 1)) {
+            atomicOr(p.err, kDevErrTimeout);
+            break;
+          }
         }
       }
+      __syncwarp();
     }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     return;
   }
 
@@ -251,12 +281,15 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
       if (grp * 16 >= valid) break;
       const int key0 = tile_start + grp * 16;  // absolute position of key row 0 of this group
 
-      // ---- S^T = K Q^T
-      float sacc[NT][4];
+      // ---- S^T = K Q^T (NACC independent accumulator chains, summed afterwards)
+      constexpr int NACC = NT == 1 ? 2 : 1;
+      float sacc2[NACC][NT][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+      for (int a = 0; a < NACC; ++a)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sacc[nt][k] = 0.f;
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) sacc2[a][nt][k] = 0.f;
       const int r0 = grp * 16 + g8;
 #pragma unroll
       for (int bx = 0; bx < NBOX; ++bx) {
@@ -284,7 +317,8 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
                 a3 = e5m2_bytes_to_f16x2<2, 3>(w1[w]);
               }
 #pragma unroll
-              for (int nt = 0; nt < NT; ++nt) mma_16816(sacc[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+              for (int nt = 0; nt < NT; ++nt)
+                mma_16816(sacc2[w % NACC][nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
             }
           } else {
 #pragma unroll
@@ -292,11 +326,22 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
               const int ks = (2 * bx + h) * 2 + u;
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt)
-                mma_16816(sacc[nt], w0[2 * u], w1[2 * u], w0[2 * u + 1], w1[2 * u + 1], qf[ks][nt][0], qf[ks][nt][1]);
+                mma_16816(sacc2[u % NACC][nt], w0[2 * u], w1[2 * u], w0[2 * u + 1], w1[2 * u + 1], qf[ks][nt][0],
+                          qf[ks][nt][1]);
             }
           }
         }
       }
+      float sacc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float v = sacc2[0][nt][k];
+#pragma unroll
+          for (int a = 1; a < NACC; ++a) v += sacc2[a][nt][k];
+          sacc[nt][k] = v;
+        }
 
       // ---- scale, mask, running max
       const bool need_mask = (key0 + 15 > min_lim);
@@ -421,6 +466,9 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
+
+  // let the merge kernel (launched with programmatic serialisation) start while this CTA finishes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ------------------------------------------------------------------ combine the token slices
   // full row sums of this warp

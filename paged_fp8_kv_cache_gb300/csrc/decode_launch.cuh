@@ -2,19 +2,36 @@
 // decode_fp16.cu, decode_e4m3.cu and decode_e5m2.cu, compiled in parallel).
 #pragma once
 
+#include <atomic>
+
 #include "decode_kernel.cuh"
 
 namespace pfkv {
+
+// The opt-in shared-memory limit is set once per device and instantiation
+// (to the largest request this library makes), not on every launch.
+template <int D, int KV, int NT>
+static cudaError_t ensure_smem_attr() {
+  static std::atomic<uint64_t> done_mask{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = uint64_t(1) << (dev & 63);
+  if (done_mask.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  const int smem = decode_smem_bytes<D, KV, NT>(8) + 1024;  // 8 consumer warps: the largest CTA
+  e = cudaFuncSetAttribute(decode_kernel<D, KV, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) done_mask.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 template <int D, int KV, int NT>
 static cudaError_t launch_one(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p, dim3 grid,
                               cudaStream_t stream) {
   const int ncw = p.nrg * p.nts;
   const int smem = decode_smem_bytes<D, KV, NT>(ncw) + 1024;
-  auto kern = decode_kernel<D, KV, NT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem_attr<D, KV, NT>();
   if (e != cudaSuccess) return e;
-  kern<<<grid, (ncw + 1) * 32, smem, stream>>>(tmk, tmv, p);
+  decode_kernel<D, KV, NT><<<grid, (ncw + 1) * 32, smem, stream>>>(tmk, tmv, p);
   return cudaGetLastError();
 }
 
@@ -22,7 +39,7 @@ template <int D, int KV, int NT>
 static int ctas_one(int ncw) {
   const int smem = decode_smem_bytes<D, KV, NT>(ncw) + 1024;
   auto kern = decode_kernel<D, KV, NT>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 1;
+  if (ensure_smem_attr<D, KV, NT>() != cudaSuccess) return 1;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, (ncw + 1) * 32, smem) != cudaSuccess) return 1;
   return n > 0 ? n : 1;

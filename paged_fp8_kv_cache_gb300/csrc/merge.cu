@@ -3,8 +3,13 @@
 // improvements"):
 //   M = max_s lse_s, w_s = exp(lse_s - M),
 //   out = sum_s w_s o_s / sum_s w_s, lse = M + ln(sum_s w_s).
-// Each thread owns 4 consecutive head-dim elements of one row; the row's
-// part LSEs are read by every thread of the row (they stay in L1).
+//
+// One warp per output row. The lanes first load the row's part LSEs in
+// parallel and reduce their maximum with shuffles, then each lane
+// accumulates its D/32 output elements over the parts, issuing the loads of
+// up to 16 parts before using any. When launched after the decode kernel with programmatic stream
+// serialisation, the grid starts while the decode kernel drains and waits
+// (griddepcontrol.wait) before touching the partials.
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
@@ -12,16 +17,21 @@
 
 namespace pfkv {
 
-__global__ void __launch_bounds__(256) lse_merge_kernel(__half* __restrict__ out, float* __restrict__ lse,
+template <int D>
+__global__ void __launch_bounds__(128) lse_merge_kernel(__half* __restrict__ out, float* __restrict__ lse,
                                                         const float* __restrict__ o_parts,
                                                         const float* __restrict__ lse_parts, int rows, int num_parts,
-                                                        int head_dim, const int32_t* __restrict__ seq_lens,
-                                                        int rows_per_seq, int split_tokens, int len_cap) {
-  const int q4 = head_dim / 4;
-  const int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-  if (idx >= static_cast<int64_t>(rows) * q4) return;
-  const int r = static_cast<int>(idx / q4);
-  const int d = static_cast<int>(idx - static_cast<int64_t>(r) * q4) * 4;
+                                                        const int32_t* __restrict__ seq_lens, int rows_per_seq,
+                                                        int split_tokens, int len_cap) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // 32 threads per row, each owning D/32 consecutive output elements; the
+  // loads of up to kBatch parts are all issued before any is used, so a row
+  // costs one memory round trip per kBatch parts.
+  constexpr int PER = D / 32;  // 4 or 8 floats
+  constexpr int kBatch = 16;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= rows) return;
   int n = num_parts;
   if (seq_lens != nullptr) {
     int len = seq_lens[r / rows_per_seq];
@@ -30,13 +40,79 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(__half* __restrict__ out
     if (n <= 1) return;  // written directly by the decode kernel
   }
   const float* lp = lse_parts + static_cast<int64_t>(r) * num_parts;
+  const float* op = o_parts + static_cast<int64_t>(r) * num_parts * D + lane * PER;
   float M = -CUDART_INF_F;
-  for (int s = 0; s < n; ++s) M = fmaxf(M, lp[s]);
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, lp[s]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  float W = 0.f;
+  if (M != -CUDART_INF_F) {
+    for (int s0 = 0; s0 < n; s0 += kBatch) {
+      float4 v[kBatch][PER / 4];
+      float l[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (s0 + u < n) {
+          l[u] = lp[s0 + u];
+#pragma unroll
+          for (int i = 0; i < PER / 4; ++i)
+            v[u][i] = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(s0 + u) * D + 4 * i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (s0 + u < n) {
+          const float w = (l[u] == -CUDART_INF_F) ? 0.f : expf(l[u] - M);
+          W += w;
+#pragma unroll
+          for (int i = 0; i < PER / 4; ++i) {
+            acc[4 * i + 0] += w * v[u][i].x;
+            acc[4 * i + 1] += w * v[u][i].y;
+            acc[4 * i + 2] += w * v[u][i].z;
+            acc[4 * i + 3] += w * v[u][i].w;
+          }
+        }
+      }
+    }
+  }
+  const bool has = (M != -CUDART_INF_F) && (W > 0.f);
+  const float inv = has ? 1.f / W : 0.f;
+  __half* orow = out + static_cast<int64_t>(r) * D + lane * PER;
+#pragma unroll
+  for (int i = 0; i < PER / 4; ++i) {
+    const __half2 h01 = __floats2half2_rn(acc[4 * i + 0] * inv, acc[4 * i + 1] * inv);
+    const __half2 h23 = __floats2half2_rn(acc[4 * i + 2] * inv, acc[4 * i + 3] * inv);
+    uint2 packed;
+    packed.x = *reinterpret_cast<const uint32_t*>(&h01);
+    packed.y = *reinterpret_cast<const uint32_t*>(&h23);
+    *reinterpret_cast<uint2*>(orow + 4 * i) = packed;
+  }
+  if (lane == 0 && lse != nullptr) lse[r] = has ? M + logf(W) : -CUDART_INF_F;
+}
+
+// Generic head dims (multiples of 4 up to 1024, standalone entry point only):
+// one thread per 4 output elements.
+__global__ void __launch_bounds__(256) lse_merge_generic_kernel(__half* __restrict__ out, float* __restrict__ lse,
+                                                                const float* __restrict__ o_parts,
+                                                                const float* __restrict__ lse_parts, int rows,
+                                                                int num_parts, int head_dim) {
+  const int q4 = head_dim / 4;
+  const int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (idx >= static_cast<int64_t>(rows) * q4) return;
+  const int r = static_cast<int>(idx / q4);
+  const int d = static_cast<int>(idx - static_cast<int64_t>(r) * q4) * 4;
+  const float* lp = lse_parts + static_cast<int64_t>(r) * num_parts;
+  float M = -CUDART_INF_F;
+  for (int s = 0; s < num_parts; ++s) M = fmaxf(M, lp[s]);
   float W = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -CUDART_INF_F) {
     const float* op = o_parts + static_cast<int64_t>(r) * num_parts * head_dim + d;
-    for (int s = 0; s < n; ++s) {
+    for (int s = 0; s < num_parts; ++s) {
       const float l = lp[s];
       if (l == -CUDART_INF_F) continue;
       const float w = expf(l - M);
@@ -63,14 +139,32 @@ cudaError_t launch_lse_merge(__half* out, float* lse, const float* o_parts, cons
                              int num_parts, int head_dim, const int32_t* seq_lens, int rows_per_seq,
                              int split_tokens, int max_seq_len, int max_len_cap, cudaStream_t stream) {
   (void)max_seq_len;
-  const int64_t total = static_cast<int64_t>(rows) * (head_dim / 4);
-  if (total == 0) return cudaSuccess;
-  const int threads = 256;
-  const int64_t blocks = (total + threads - 1) / threads;
-  lse_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      out, lse, o_parts, lse_parts, rows, num_parts, head_dim, seq_lens, rows_per_seq > 0 ? rows_per_seq : 1,
-      split_tokens > 0 ? split_tokens : 1, max_len_cap);
-  return cudaGetLastError();
+  if (rows == 0) return cudaSuccess;
+  if (head_dim != 128 && head_dim != 256) {
+    const int64_t total = static_cast<int64_t>(rows) * (head_dim / 4);
+    const int64_t blocks = (total + 255) / 256;
+    lse_merge_generic_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(out, lse, o_parts, lse_parts, rows,
+                                                                               num_parts, head_dim);
+    return cudaGetLastError();
+  }
+  const int warps = 4;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + warps - 1) / warps));
+  cfg.blockDim = dim3(32 * warps);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int rps = rows_per_seq > 0 ? rows_per_seq : 1;
+  const int st = split_tokens > 0 ? split_tokens : 1;
+  if (head_dim == 128)
+    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128>, out, lse, o_parts, lse_parts, rows, num_parts, seq_lens,
+                              rps, st, max_len_cap);
+  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<256>, out, lse, o_parts, lse_parts, rows, num_parts, seq_lens, rps,
+                            st, max_len_cap);
 }
 
 }  // namespace pfkv
