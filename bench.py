@@ -45,7 +45,7 @@ METRIC = "paged FP8-KV decode attention: effective HBM GB/s and % of GB300 peak"
 DEFAULT_WORKLOAD = 2  # the batched-decode workload (the second of the five)
 L2_FLUSH_BYTES = 256 << 20  # > 2x the 129 MB L2
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["decode_kernel.cuh", "device_utils.cuh", "frag_layout.h", "merge.cu"]
+KERNEL_SOURCES = ["decode_kernel.cuh", "device_utils.cuh", "frag_layout.h"]  # the decode kernel
 
 
 # ----------------------------------------------------------------------------- helpers

@@ -4,12 +4,11 @@
 //   M = max_s lse_s, w_s = exp(lse_s - M),
 //   out = sum_s w_s o_s / sum_s w_s, lse = M + ln(sum_s w_s).
 //
-// One warp per output row. The lanes first load the row's part LSEs in
-// parallel and reduce their maximum with shuffles, then each lane
-// accumulates its D/32 output elements over the parts, issuing the loads of
-// up to 16 parts before using any. When launched after the decode kernel with programmatic stream
-// serialisation, the grid starts while the decode kernel drains and waits
-// (griddepcontrol.wait) before touching the partials.
+// One CTA of 8 warps per output row; the row's parts are spread over the
+// warps so that a row with many split ranges still costs about one memory
+// round trip. When launched after the decode kernel with programmatic
+// stream serialisation, the grid starts while the decode kernel drains and
+// waits (griddepcontrol.wait) before touching the partials.
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
@@ -18,54 +17,64 @@
 namespace pfkv {
 
 template <int D>
-__global__ void __launch_bounds__(128) lse_merge_kernel(__half* __restrict__ out, float* __restrict__ lse,
+__global__ void __launch_bounds__(256) lse_merge_kernel(__half* __restrict__ out, float* __restrict__ lse,
                                                         const float* __restrict__ o_parts,
                                                         const float* __restrict__ lse_parts, int rows, int num_parts,
                                                         const int32_t* __restrict__ seq_lens, int rows_per_seq,
                                                         int split_tokens, int len_cap) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // 32 threads per row, each owning D/32 consecutive output elements; the
-  // loads of up to kBatch parts are all issued before any is used, so a row
-  // costs one memory round trip per kBatch parts.
-  constexpr int PER = D / 32;  // 4 or 8 floats
-  constexpr int kBatch = 16;
-  const int lane = threadIdx.x & 31;
-  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (r >= rows) return;
+  // One CTA (8 warps) per row. Warp w takes parts w, w+8, ...; each lane owns
+  // D/32 consecutive output elements. The row maximum is reduced first (all
+  // part LSEs in one pass), every warp then issues the loads of up to kBatch
+  // of its parts before using any, and the 8 warp partial sums are added
+  // through shared memory.
+  constexpr int PER = D / 32;  // 4 or 8 floats per lane
+  constexpr int kBatch = 8;
+  __shared__ float s_red[8];
+  __shared__ float s_w[8];
+  __shared__ float4 s_acc[8][D / 4];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r = blockIdx.x;
   int n = num_parts;
   if (seq_lens != nullptr) {
     int len = seq_lens[r / rows_per_seq];
     len = len < 0 ? 0 : (len > len_cap ? len_cap : len);
     n = len > 0 ? (len + split_tokens - 1) / split_tokens : 1;
-    if (n <= 1) return;  // written directly by the decode kernel
+    if (n <= 1) return;  // written directly by the decode kernel (uniform across the CTA)
   }
   const float* lp = lse_parts + static_cast<int64_t>(r) * num_parts;
   const float* op = o_parts + static_cast<int64_t>(r) * num_parts * D + lane * PER;
   float M = -CUDART_INF_F;
-  for (int s = lane; s < n; s += 32) M = fmaxf(M, lp[s]);
+  for (int s = threadIdx.x; s < n; s += blockDim.x) M = fmaxf(M, lp[s]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) s_red[warp] = M;
+  __syncthreads();
+  M = s_red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) M = fmaxf(M, s_red[w]);
 
   float acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
   float W = 0.f;
   if (M != -CUDART_INF_F) {
-    for (int s0 = 0; s0 < n; s0 += kBatch) {
+    for (int s0 = warp; s0 < n; s0 += 8 * kBatch) {
       float4 v[kBatch][PER / 4];
       float l[kBatch];
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
-        if (s0 + u < n) {
-          l[u] = lp[s0 + u];
+        const int s = s0 + 8 * u;
+        if (s < n) {
+          l[u] = lp[s];
 #pragma unroll
           for (int i = 0; i < PER / 4; ++i)
-            v[u][i] = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(s0 + u) * D + 4 * i);
+            v[u][i] = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(s) * D + 4 * i);
         }
       }
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
-        if (s0 + u < n) {
+        if (s0 + 8 * u < n) {
           const float w = (l[u] == -CUDART_INF_F) ? 0.f : expf(l[u] - M);
           W += w;
 #pragma unroll
@@ -79,19 +88,34 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(__half* __restrict__ out
       }
     }
   }
-  const bool has = (M != -CUDART_INF_F) && (W > 0.f);
-  const float inv = has ? 1.f / W : 0.f;
-  __half* orow = out + static_cast<int64_t>(r) * D + lane * PER;
 #pragma unroll
-  for (int i = 0; i < PER / 4; ++i) {
-    const __half2 h01 = __floats2half2_rn(acc[4 * i + 0] * inv, acc[4 * i + 1] * inv);
-    const __half2 h23 = __floats2half2_rn(acc[4 * i + 2] * inv, acc[4 * i + 3] * inv);
+  for (int i = 0; i < PER / 4; ++i)
+    s_acc[warp][lane * (PER / 4) + i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+  if (lane == 0) s_w[warp] = W;
+  __syncthreads();
+  // 256 threads finish D / 4 float4 outputs (D = 128: 32 threads, D = 256: 64 threads)
+  if (threadIdx.x < D / 4) {
+    float Wt = 0.f;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      Wt += s_w[w];
+      const float4 x = s_acc[w][threadIdx.x];
+      a.x += x.x;
+      a.y += x.y;
+      a.z += x.z;
+      a.w += x.w;
+    }
+    const bool has = (M != -CUDART_INF_F) && (Wt > 0.f);
+    const float inv = has ? 1.f / Wt : 0.f;
+    const __half2 h01 = __floats2half2_rn(a.x * inv, a.y * inv);
+    const __half2 h23 = __floats2half2_rn(a.z * inv, a.w * inv);
     uint2 packed;
     packed.x = *reinterpret_cast<const uint32_t*>(&h01);
     packed.y = *reinterpret_cast<const uint32_t*>(&h23);
-    *reinterpret_cast<uint2*>(orow + 4 * i) = packed;
+    *reinterpret_cast<uint2*>(out + static_cast<int64_t>(r) * D + 4 * threadIdx.x) = packed;
+    if (threadIdx.x == 0 && lse != nullptr) lse[r] = has ? M + logf(Wt) : -CUDART_INF_F;
   }
-  if (lane == 0 && lse != nullptr) lse[r] = has ? M + logf(W) : -CUDART_INF_F;
 }
 
 // Generic head dims (multiples of 4 up to 1024, standalone entry point only):
@@ -147,10 +171,9 @@ cudaError_t launch_lse_merge(__half* out, float* lse, const float* o_parts, cons
                                                                                num_parts, head_dim);
     return cudaGetLastError();
   }
-  const int warps = 4;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((rows + warps - 1) / warps));
-  cfg.blockDim = dim3(32 * warps);
+  cfg.gridDim = dim3(static_cast<unsigned>(rows));
+  cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
