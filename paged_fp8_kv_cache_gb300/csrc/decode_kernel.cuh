@@ -74,6 +74,9 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
   const int ncw = p.nrg * p.nts;
   const int R = p.T * p.G;
 
+  // launched with programmatic stream serialisation: wait for the preceding
+  // grid (which may produce q, the cache or the tables) before any global read
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // sequence length, validated against what the block table can address
   int N = p.seq_lens[b];
   {

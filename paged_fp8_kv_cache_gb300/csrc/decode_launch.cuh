@@ -31,8 +31,7 @@ static cudaError_t launch_one(const CUtensorMap& tmk, const CUtensorMap& tmv, co
   const int smem = decode_smem_bytes<D, KV, NT>(ncw) + 1024;
   cudaError_t e = ensure_smem_attr<D, KV, NT>();
   if (e != cudaSuccess) return e;
-  decode_kernel<D, KV, NT><<<grid, (ncw + 1) * 32, smem, stream>>>(tmk, tmv, p);
-  return cudaGetLastError();
+  return launch_pdl(decode_kernel<D, KV, NT>, grid, dim3((ncw + 1) * 32), smem, stream, tmk, tmv, p);
 }
 
 template <int D, int KV, int NT>

@@ -18,19 +18,6 @@
 
 namespace pfkv {
 
-cudaError_t launch_decode_fp16(const DecodeLaunch&, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, dim3,
-                               cudaStream_t);
-cudaError_t launch_decode_e4m3(const DecodeLaunch&, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, dim3,
-                               cudaStream_t);
-cudaError_t launch_decode_e5m2(const DecodeLaunch&, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, dim3,
-                               cudaStream_t);
-int decode_smem_fp16(const DecodeLaunch&, int);
-int decode_smem_e4m3(const DecodeLaunch&, int);
-int decode_smem_e5m2(const DecodeLaunch&, int);
-int decode_ctas_fp16(const DecodeLaunch&, int);
-int decode_ctas_e4m3(const DecodeLaunch&, int);
-int decode_ctas_e5m2(const DecodeLaunch&, int);
-
 __device__ unsigned g_pfkv_err;  // per-device error word (PFKV_DEVERR_* bits)
 
 namespace {
@@ -173,19 +160,36 @@ int log2i(int x) {
 
 struct Plan {
   DecodeLaunch cfg;
-  int nrg, nts, ncw;
+  int nrg, nts, ncw;  // mma.sync decode kernel: row groups x key slices of consumer warps
+  bool tc;            // tcgen05 grouped-verify kernel (FP8 cache, more than 16 rows per KV head)
+  int nmax;           // its padded row count (32, 48, 64)
+  int tile;           // keys per pipeline tile (split ranges are multiples of it)
   int splits, split_tokens;
 };
 
-int ctas_per_sm(int dev, const DecodeLaunch& cfg, int ncw) {
-  const long long key = (((static_cast<long long>(dev) * 4 + cfg.kv) * 512 + cfg.head_dim) * 4 + cfg.nt) * 64 + ncw;
+int ctas_per_sm(int dev, const DecodeLaunch& cfg, int ncw, bool tc, int nmax) {
+  const long long key =
+      ((((static_cast<long long>(dev) * 4 + cfg.kv) * 512 + cfg.head_dim) * 4 + cfg.nt) * 64 + ncw) * 256 +
+      (tc ? nmax : 0);
   {
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_occ.find(key);
     if (it != g_occ.end()) return it->second;
   }
-  int n = cfg.kv == kKvFp16 ? decode_ctas_fp16(cfg, ncw)
-                            : (cfg.kv == kKvE4m3 ? decode_ctas_e4m3(cfg, ncw) : decode_ctas_e5m2(cfg, ncw));
+  int n = 1;
+  if (tc) {
+    CUtensorMap unused;
+    std::memset(&unused, 0, sizeof(unused));
+    DecodeParams none;
+    std::memset(&none, 0, sizeof(none));
+    if (cfg.kv == kKvE4m3)
+      launch_verify_e4m3(cfg.head_dim, nmax, unused, unused, none, dim3(1), nullptr, &n);
+    else
+      launch_verify_e5m2(cfg.head_dim, nmax, unused, unused, none, dim3(1), nullptr, &n);
+  } else {
+    n = cfg.kv == kKvFp16 ? decode_ctas_fp16(cfg, ncw)
+                          : (cfg.kv == kKvE4m3 ? decode_ctas_e4m3(cfg, ncw) : decode_ctas_e5m2(cfg, ncw));
+  }
   std::lock_guard<std::mutex> lk(g_mu);
   g_occ[key] = n;
   return n;
@@ -220,7 +224,10 @@ pfkv_status make_plan(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_k
   pl->nrg = (R + rows_w - 1) / rows_w;
   pl->nts = pl->nrg == 1 ? 4 : 2;
   pl->ncw = pl->nrg * pl->nts;
-  const int tiles = max_seq_len > 0 ? (max_seq_len + kTileKeys - 1) / kTileKeys : 1;
+  pl->tc = (dtype != PFKV_KV_FP16) && R > 16;
+  pl->nmax = R <= 32 ? 32 : (R <= 48 ? 48 : 64);
+  pl->tile = pl->tc ? 128 : kTileKeys;
+  const int tiles = max_seq_len > 0 ? (max_seq_len + pl->tile - 1) / pl->tile : 1;
   int want;
   if (num_splits_request > 0) {
     want = num_splits_request;
@@ -230,7 +237,7 @@ pfkv_status make_plan(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_k
     if (e == cudaSuccess) e = sm_count(dev, &sms);
     if (e != cudaSuccess) return cuda_fail(e, "device query");
     const int units = num_seqs > 0 ? num_seqs * Hkv : 1;
-    const int target = sms * ctas_per_sm(dev, pl->cfg, pl->ncw);
+    const int target = sms * ctas_per_sm(dev, pl->cfg, pl->ncw, pl->tc, pl->nmax);
     const int base = (target + units - 1) / units;
     // bound the keys per CTA so ragged batches balance; the bound grows with
     // the row count because every range costs an fp32 partial per row
@@ -242,7 +249,7 @@ pfkv_status make_plan(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_k
   if (want < 1) want = 1;
   if (want > tiles) want = tiles;
   const int tiles_per_split = (tiles + want - 1) / want;
-  pl->split_tokens = tiles_per_split * kTileKeys;
+  pl->split_tokens = tiles_per_split * pl->tile;
   pl->splits = (tiles + tiles_per_split - 1) / tiles_per_split;
   return PFKV_OK;
 }
@@ -422,9 +429,14 @@ pfkv_status pfkv_paged_attention_decode(void* out, float* lse, const void* q, co
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   dim3 grid(pl.splits, num_kv_heads, num_seqs);
-  e = kv == kKvFp16 ? launch_decode_fp16(pl.cfg, tmk, tmv, p, grid, s)
-                    : (kv == kKvE4m3 ? launch_decode_e4m3(pl.cfg, tmk, tmv, p, grid, s)
-                                     : launch_decode_e5m2(pl.cfg, tmk, tmv, p, grid, s));
+  if (pl.tc) {
+    e = kv == kKvE4m3 ? launch_verify_e4m3(head_dim, pl.nmax, tmk, tmv, p, grid, s, nullptr)
+                      : launch_verify_e5m2(head_dim, pl.nmax, tmk, tmv, p, grid, s, nullptr);
+  } else {
+    e = kv == kKvFp16 ? launch_decode_fp16(pl.cfg, tmk, tmv, p, grid, s)
+                      : (kv == kKvE4m3 ? launch_decode_e4m3(pl.cfg, tmk, tmv, p, grid, s)
+                                       : launch_decode_e5m2(pl.cfg, tmk, tmv, p, grid, s));
+  }
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (pl.splits > 1) {
     const long long cap_ll = static_cast<long long>(max_blocks_per_seq) * page_size;

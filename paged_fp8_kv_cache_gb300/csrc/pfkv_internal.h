@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace pfkv {
 
 enum KvKind : int { kKvFp16 = 0, kKvE4m3 = 1, kKvE5m2 = 2 };
@@ -50,13 +52,43 @@ struct DecodeLaunch {
   int nt;  // n-tiles of 8 query rows per consumer warp (1 or 2)
 };
 
-// decode_*.cu
-cudaError_t launch_decode(const DecodeLaunch& cfg, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                          const DecodeParams& p, dim3 grid, cudaStream_t stream);
-// Dynamic shared memory and threads per CTA of a decode configuration.
-int decode_smem_request(const DecodeLaunch& cfg, int ncw);
-// CTAs of this configuration that fit on one SM (cached per device).
-int decode_ctas_per_sm(const DecodeLaunch& cfg, int ncw);
+// Launch with programmatic stream serialisation: the grid may start while the
+// previous kernel on the stream drains; the kernel executes griddepcontrol.wait
+// before reading anything that kernel could have written.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, int smem, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// decode_fp16.cu / decode_e4m3.cu / decode_e5m2.cu: the mma.sync decode kernel per cache
+// dtype; *_ctas_* returns the CTAs of a configuration that fit on one SM.
+cudaError_t launch_decode_fp16(const DecodeLaunch&, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, dim3,
+                               cudaStream_t);
+cudaError_t launch_decode_e4m3(const DecodeLaunch&, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, dim3,
+                               cudaStream_t);
+cudaError_t launch_decode_e5m2(const DecodeLaunch&, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, dim3,
+                               cudaStream_t);
+int decode_ctas_fp16(const DecodeLaunch&, int ncw);
+int decode_ctas_e4m3(const DecodeLaunch&, int ncw);
+int decode_ctas_e5m2(const DecodeLaunch&, int ncw);
+
+// verify_e4m3.cu / verify_e5m2.cu: tcgen05 grouped verify (FP8 caches). nmax = rows padded
+// to 32/48/64. With ctas_out non-null nothing is launched: it receives the CTAs per SM.
+cudaError_t launch_verify_e4m3(int head_dim, int nmax, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                               const DecodeParams& p, dim3 grid, cudaStream_t stream, int* ctas_out);
+cudaError_t launch_verify_e5m2(int head_dim, int nmax, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                               const DecodeParams& p, dim3 grid, cudaStream_t stream, int* ctas_out);
 
 // merge.cu: combine per-range partials. If seq_lens is non-null, row r of
 // sequence b = r / (T * num_q_heads) has ceil(seq_len / split_tokens) parts
