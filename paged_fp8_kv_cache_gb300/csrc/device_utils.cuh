@@ -9,10 +9,14 @@
 
 namespace pfkv {
 
-// Upper bound on polls of one mbarrier wait. Each poll may suspend the
-// thread for a hardware-defined interval, so this is seconds of waiting for
-// a copy that never lands; the kernel then reports PFKV_DEVERR_TIMEOUT.
-constexpr uint32_t kWaitPollLimit = 1u << 22;
+// Bound on one mbarrier wait, in wall-clock time: a copy or an arrival that
+// has not landed after this long never will, and the kernel then reports
+// PFKV_DEVERR_TIMEOUT instead of spinning on.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// Suspend-time hint of one try_wait: the waiting thread is descheduled until
+// the phase completes or this many nanoseconds pass, so idle warps do not
+// take issue slots from working ones.
+constexpr uint32_t kWaitHintNs = 1000000u;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -37,22 +41,47 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(addr), "r"(parity), "r"(kWaitHintNs)
+      : "memory");
+  return done != 0;
+}
+
+// Non-blocking: has the phase with parity `parity` of `bar` completed?
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Wait until the phase with parity `parity` of `bar` has completed.
-// Returns false if the poll limit was reached first.
+// Returns false if kWaitLimitNs passed first.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t addr = smem_u32(bar);
-  for (uint32_t i = 0; i < kWaitPollLimit; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(addr), "r"(parity)
-        : "memory");
-    if (done) return true;
+  if (mbar_try_wait(addr, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(addr, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) return false;
   }
-  return false;
+  return true;
 }
 
 // 2D TMA tile load (coordinates: x = innermost, in elements; y = row),

@@ -49,8 +49,6 @@ struct VerifyShape {
   static constexpr int NBOX = D / kBoxBytes;             // 128-byte boxes per FP8 key row
   static constexpr int SUB = KT * kBoxBytes;             // one box column of a tile (16 KB)
   static constexpr int KV_TILE = NBOX * SUB;             // K (or V) bytes per tile
-  static constexpr int STAGE = 2 * KV_TILE;
-  static constexpr int NSTG = STAGE <= 32768 ? 3 : 2;    // ring depth
   static constexpr int NMAX = NMAX_;                     // padded query rows (MMA N): 32, 48 or 64
   static constexpr int Q_BYTES = (D / 64) * NMAX * 128;  // Q as K-major 128B-swizzled blocks of 64 dims
   static constexpr int PT_BYTES = (KT / 64) * NMAX * 128;  // one P^T buffer (K-major, 64-key blocks)
@@ -61,13 +59,22 @@ struct VerifyShape {
   static constexpr int COL_AK = ((COL_O + MT * NMAX + 31) / 32) * 32;  // D/2: K as A operand (fp16 pairs)
   static constexpr int COL_AV = COL_AK + D / 2;          // MT x KT/2: V^T as A operand
   static_assert(COL_AV + MT * KT / 2 <= TMEM_COLS, "TMEM budget");
-  // shared memory map (offsets from the 1 KB-aligned base)
-  static constexpr int OFF_RING = 0;
-  static constexpr int OFF_Q = OFF_RING + NSTG * STAGE;
-  static constexpr int OFF_PT = OFF_Q + Q_BYTES;  // 2 buffers
-  static constexpr int OFF_MISC = OFF_PT + 2 * PT_BYTES;
   // misc: m_ref, alpha, wred[4], lsum[4], m_prev (NMAX floats each), flags, TMEM slot, barriers
   static constexpr int MISC_BYTES = 11 * NMAX * 4 + 64 + 32 * 8;
+  // Separate K and V rings. V tiles are held longest (the V operand of tile i+1 can only be
+  // written once the PV MMAs of tile i are done), so the V ring gets whatever depth the
+  // remaining shared memory allows (2..4 tiles).
+  static constexpr int kSmemLimit = 227 * 1024;
+  static constexpr int NK = KV_TILE <= 16384 ? 3 : 2;
+  static constexpr int NV_FIT = (kSmemLimit - 1024 - NK * KV_TILE - Q_BYTES - 2 * PT_BYTES - MISC_BYTES) / KV_TILE;
+  static constexpr int NV = NV_FIT > 4 ? 4 : NV_FIT;
+  static_assert(NV >= 2, "shared memory budget");
+  // shared memory map (offsets from the 1 KB-aligned base)
+  static constexpr int OFF_KRING = 0;
+  static constexpr int OFF_VRING = OFF_KRING + NK * KV_TILE;
+  static constexpr int OFF_Q = OFF_VRING + NV * KV_TILE;
+  static constexpr int OFF_PT = OFF_Q + Q_BYTES;  // 2 buffers
+  static constexpr int OFF_MISC = OFF_PT + 2 * PT_BYTES;
   static constexpr int SMEM = OFF_MISC + MISC_BYTES;
 };
 
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(448, 1)
     verify_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeParams p) {
   using S = VerifyShape<D, NMAX_>;
-  constexpr int KT = S::KT, NBOX = S::NBOX, NSTG = S::NSTG, NMAX = S::NMAX, MT = S::MT;
+  constexpr int KT = S::KT, NBOX = S::NBOX, NK = S::NK, NV = S::NV, NMAX = S::NMAX, MT = S::MT;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -177,9 +184,11 @@ __global__ void __launch_bounds__(448, 1)
   int* flag = reinterpret_cast<int*>(m_prev + NMAX);             // [3] rescale votes
   uint32_t* tslot = reinterpret_cast<uint32_t*>(flag + 4);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_MISC + 11 * NMAX * 4 + 64);
-  uint64_t* full = bars;               // [NSTG] producer -> converters
-  uint64_t* empty = full + NSTG;       // [NSTG] converters -> producer
-  uint64_t* ak_full = empty + NSTG;    // K converter -> MMA (K operand written)
+  uint64_t* kfull = bars;              // [NK] producer -> K converter
+  uint64_t* kempty = kfull + NK;       // [NK] K converter -> producer
+  uint64_t* vfull = kempty + NK;       // [NV] producer -> V converter
+  uint64_t* vempty = vfull + NV;       // [NV] V converter -> producer
+  uint64_t* ak_full = vempty + NV;     // K converter -> MMA (K operand written)
   uint64_t* av_full = ak_full + 1;     // V converter -> MMA (V operand written)
   uint64_t* ak_free = av_full + 1;     // MMA commit: S^T MMAs done with the K operand
   uint64_t* s_full = ak_free + 1;      // [2] MMA commit: S^T ready
@@ -193,9 +202,13 @@ __global__ void __launch_bounds__(448, 1)
   const int tid = threadIdx.x;
 
   if (tid == 0) {
-    for (int s = 0; s < NSTG; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 8);  // one arrival per converter warp (both warpgroups)
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 4);  // one arrival per K-converter warp
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], 4);  // one arrival per V-converter warp
     }
     mbar_init(ak_full, 4);
     mbar_init(av_full, 4);
@@ -269,61 +282,69 @@ __global__ void __launch_bounds__(448, 1)
         }
         return __shfl_sync(0xffffffffu, my_id, pidx - chunk_base);
       };
-      for (int it = 0; it < ntiles; ++it) {
-        const int s = it % NSTG;
-        if (it >= NSTG) {
-          bool got = true;
-          if (lane == 0) got = mbar_wait(&empty[s], ((it / NSTG) - 1) & 1);
-          got = __shfl_sync(0xffffffffu, got, 0);
-          if (!got) {
+      // rows of the tile's 64-row boxes (P >= 64) or pages (P < 64); at most 8
+      auto wait_slot = [&](uint64_t* bar, int it, int depth) -> bool {
+        if (it < depth) return true;
+        bool got = true;
+        if (lane == 0) got = mbar_wait(&bar[it % depth], ((it / depth) - 1) & 1);
+        return __shfl_sync(0xffffffffu, got, 0);
+      };
+      for (int it = 0; it < ntiles && alive; ++it) {
+        const int tile_start = t0 + it * KT;
+        const int valid = min(KT, t1 - tile_start);
+        int rows[8], box_rows, nbox_rows;
+        if (P >= kTileKeys) {
+          nbox_rows = (valid + kTileKeys - 1) / kTileKeys;
+          box_rows = kTileKeys;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int key = tile_start + hf * kTileKeys;
+            rows[hf] = 0;
+            if (hf < nbox_rows) rows[hf] = (page_id(key >> p.page_shift) * p.num_kv_heads + kvh) * P + (key & (P - 1));
+          }
+        } else {
+          nbox_rows = (valid + P - 1) >> p.page_shift;
+          box_rows = P;
+          const int pfirst = tile_start >> p.page_shift;
+#pragma unroll
+          for (int pg = 0; pg < 8; ++pg) {
+            rows[pg] = 0;
+            if (pg < nbox_rows) rows[pg] = (page_id(pfirst + pg) * p.num_kv_heads + kvh) * P;
+          }
+        }
+        const uint32_t bytes = NBOX * nbox_rows * box_rows * kBoxBytes;
+        // K tile, then V tile, each into its own ring
+        for (int which = 0; which < 2; ++which) {
+          uint64_t* fullb = which == 0 ? kfull : vfull;
+          uint64_t* emptyb = which == 0 ? kempty : vempty;
+          const int depth = which == 0 ? NK : NV;
+          if (!wait_slot(emptyb, it, depth)) {
             if (lane == 0) atomicOr(p.err, kDevErrTimeout);
             alive = false;
             break;
           }
-        }
-        unsigned char* kdst = smem + S::OFF_RING + s * S::STAGE;
-        unsigned char* vdst = kdst + S::KV_TILE;
-        const int tile_start = t0 + it * KT;
-        const int valid = min(KT, t1 - tile_start);
-        if (P >= kTileKeys) {
-          // 64-row boxes: one page (or part of one) per half tile
-          const int halves = (valid + kTileKeys - 1) / kTileKeys;
-          if (lane == 0) mbar_arrive_expect_tx(&full[s], 2 * NBOX * halves * kTileKeys * kBoxBytes);
-          for (int hf = 0; hf < halves; ++hf) {
-            const int key = tile_start + hf * kTileKeys;
-            const int blk = page_id(key >> p.page_shift);
-            const int row = (blk * p.num_kv_heads + kvh) * P + (key & (P - 1));
-            if (lane == 0) {
+          unsigned char* dst = smem + (which == 0 ? S::OFF_KRING : S::OFF_VRING) + (it % depth) * S::KV_TILE;
+          const CUtensorMap* map = which == 0 ? &tmk : &tmv;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&fullb[it % depth], bytes);
+            for (int r = 0; r < nbox_rows; ++r) {
 #pragma unroll
-              for (int bx = 0; bx < NBOX; ++bx) {
-                const int off = bx * S::SUB + hf * kTileKeys * kBoxBytes;
-                tma_load_2d(kdst + off, &tmk, &full[s], bx * kBoxBytes, row);
-                tma_load_2d(vdst + off, &tmv, &full[s], bx * kBoxBytes, row);
-              }
-            }
-          }
-        } else {
-          const int npages = (valid + P - 1) >> p.page_shift;
-          const int pfirst = tile_start >> p.page_shift;
-          if (lane == 0) mbar_arrive_expect_tx(&full[s], 2 * NBOX * npages * P * kBoxBytes);
-          for (int pg = 0; pg < npages; ++pg) {
-            const int blk = page_id(pfirst + pg);
-            const int row = (blk * p.num_kv_heads + kvh) * P;
-            if (lane == 0) {
-#pragma unroll
-              for (int bx = 0; bx < NBOX; ++bx) {
-                const int off = bx * S::SUB + pg * P * kBoxBytes;
-                tma_load_2d(kdst + off, &tmk, &full[s], bx * kBoxBytes, row);
-                tma_load_2d(vdst + off, &tmv, &full[s], bx * kBoxBytes, row);
-              }
+              for (int bx = 0; bx < NBOX; ++bx)
+                tma_load_2d(dst + bx * S::SUB + r * box_rows * kBoxBytes, map, &fullb[it % depth], bx * kBoxBytes,
+                            rows[r]);
             }
           }
         }
       }
       // do not leave while copies may still land in this CTA's shared memory
       if (lane == 0) {
-        for (int it = max(0, ntiles - NSTG); it < ntiles; ++it)
-          if (!mbar_wait(&full[it % NSTG], (it / NSTG) & 1)) {
+        for (int it = max(0, ntiles - NK); it < ntiles; ++it)
+          if (!mbar_wait(&kfull[it % NK], (it / NK) & 1)) {
+            atomicOr(p.err, kDevErrTimeout);
+            break;
+          }
+        for (int it = max(0, ntiles - NV); it < ntiles; ++it)
+          if (!mbar_wait(&vfull[it % NV], (it / NV) & 1)) {
             atomicOr(p.err, kDevErrTimeout);
             break;
           }
@@ -336,41 +357,54 @@ __global__ void __launch_bounds__(448, 1)
       const uint32_t idesc = umma_idesc_f16(NP);
       const uint32_t q_base = smem_u32(smem + S::OFF_Q);
       const uint32_t pt_base = smem_u32(smem + S::OFF_PT);
-      auto issue_s = [&](int i) -> bool {
-        if (!mbar_wait(ak_full, i & 1)) return false;
-        if (i >= 2 && !mbar_wait(&s_free[i & 1], ((i >> 1) - 1) & 1)) return false;
-        tc_fence_after();
-        const uint32_t d_t = tbase + S::COL_S + (i & 1) * NMAX;
+      // Issue whichever MMA group is ready: S^T of the next tile (its K operand written, its
+      // S buffer released by the softmax) or O^T of the oldest tile whose V operand and P^T
+      // are written. Neither waits behind the other.
+      int sn = 0, on = 0;
+      bool ok = true;
+      uint64_t last = global_ns();
+      while (on < ntiles) {
+        bool progress = false;
+        if (sn < ntiles && mbar_test(ak_full, sn & 1) &&
+            (sn < 2 || mbar_test(&s_free[sn & 1], ((sn >> 1) - 1) & 1))) {
+          tc_fence_after();
+          const uint32_t d_t = tbase + S::COL_S + (sn & 1) * NMAX;
 #pragma unroll 1
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t bd = umma_desc_sw128(q_base + (ks >> 2) * NMAX * 128 + (ks & 3) * 32);
-          umma_ts(d_t, tbase + S::COL_AK + 8 * ks, bd, idesc, ks > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[i & 1]);
-        umma_commit(ak_free);
-        return true;
-      };
-      // S^T of tile i+1 is issued before O^T of tile i so that the softmax of i+1 overlaps it
-      bool ok = issue_s(0);
-      for (int i = 0; i < ntiles && ok; ++i) {
-        if (i + 1 < ntiles && !(ok = issue_s(i + 1))) break;
-        if (!mbar_wait(av_full, i & 1) || !mbar_wait(&pt_full[i & 1], (i >> 1) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t pt = pt_base + (i & 1) * S::PT_BYTES;
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll 1
-          for (int ks = 0; ks < KT / 16; ++ks) {
-            const uint64_t bd = umma_desc_sw128(pt + (ks >> 2) * NMAX * 128 + (ks & 3) * 32);
-            umma_ts(tbase + S::COL_O + mt * NMAX, tbase + S::COL_AV + mt * (KT / 2) + 8 * ks, bd, idesc,
-                    (i > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint64_t bd = umma_desc_sw128(q_base + (ks >> 2) * NMAX * 128 + (ks & 3) * 32);
+            umma_ts(d_t, tbase + S::COL_AK + 8 * ks, bd, idesc, ks > 0 ? 1u : 0u);
           }
+          umma_commit(&s_full[sn & 1]);
+          umma_commit(ak_free);
+          ++sn;
+          progress = true;
         }
-        umma_commit(&pt_free[i & 1]);
-        umma_commit(o_done);
+        if (on < sn && mbar_test(av_full, on & 1) && mbar_test(&pt_full[on & 1], (on >> 1) & 1)) {
+          tc_fence_after();
+          const uint32_t pt = pt_base + (on & 1) * S::PT_BYTES;
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll 1
+            for (int ks = 0; ks < KT / 16; ++ks) {
+              const uint64_t bd = umma_desc_sw128(pt + (ks >> 2) * NMAX * 128 + (ks & 3) * 32);
+              umma_ts(tbase + S::COL_O + mt * NMAX, tbase + S::COL_AV + mt * (KT / 2) + 8 * ks, bd, idesc,
+                      (on > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
+          umma_commit(&pt_free[on & 1]);
+          umma_commit(o_done);
+          ++on;
+          progress = true;
+        }
+        if (progress) {
+          last = global_ns();
+        } else {
+          if (global_ns() - last > kWaitLimitNs) {
+            ok = false;
+            break;
+          }
+          __nanosleep(32);
+        }
       }
       if (!ok) atomicOr(p.err, kDevErrTimeout);
     }
@@ -381,13 +415,13 @@ __global__ void __launch_bounds__(448, 1)
     const int key_row = 32 * q + lane;   // this thread's key of the tile = its TMEM lane
     const uint32_t tq = tbase + (static_cast<uint32_t>(32 * q) << 16);
     for (int it = 0; it < ntiles; ++it) {
-      const int s = it % NSTG;
-      if (!mbar_wait(&full[s], (it / NSTG) & 1) || (it > 0 && !mbar_wait(ak_free, (it - 1) & 1))) {
+      const int s = it % NK;
+      if (!mbar_wait(&kfull[s], (it / NK) & 1) || (it > 0 && !mbar_wait(ak_free, (it - 1) & 1))) {
         alive = false;
         break;
       }
       tc_fence_after();
-      const unsigned char* Ks = smem + S::OFF_RING + s * S::STAGE;
+      const unsigned char* Ks = smem + S::OFF_KRING + s * S::KV_TILE;
 #pragma unroll
       for (int bx = 0; bx < NBOX; ++bx) {
 #pragma unroll
@@ -411,7 +445,7 @@ __global__ void __launch_bounds__(448, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(ak_full);
-        mbar_arrive(&empty[s]);
+        mbar_arrive(&kempty[s]);
       }
     }
     if (!alive && lane == 0) atomicOr(p.err, kDevErrTimeout);
@@ -429,13 +463,13 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
     for (int j = 0; j < 8; ++j) voff[j] = vbx * S::SUB + swz_offset(j, vbyte >> 4) + (vbyte & 15);
     for (int it = 0; it < ntiles; ++it) {
-      const int s = it % NSTG;
-      if (!mbar_wait(&full[s], (it / NSTG) & 1) || (it > 0 && !mbar_wait(o_done, (it - 1) & 1))) {
+      const int s = it % NV;
+      if (!mbar_wait(&vfull[s], (it / NV) & 1) || (it > 0 && !mbar_wait(o_done, (it - 1) & 1))) {
         alive = false;
         break;
       }
       tc_fence_after();
-      const unsigned char* Vs = smem + S::OFF_RING + s * S::STAGE + S::KV_TILE;
+      const unsigned char* Vs = smem + S::OFF_VRING + s * S::KV_TILE;
       const int valid = min(KT, t1 - (t0 + it * KT));
       const bool tail = valid < KT;
 #pragma unroll 1
@@ -470,7 +504,7 @@ __global__ void __launch_bounds__(448, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(av_full);
-        mbar_arrive(&empty[s]);
+        mbar_arrive(&vempty[s]);
       }
     }
     if (!alive && lane == 0) atomicOr(p.err, kDevErrTimeout);
@@ -606,7 +640,8 @@ __global__ void __launch_bounds__(448, 1)
           }
         }
         if (it > 0) {
-          // rescale the O^T columns once the previous tile's MMAs are done
+          // rescale the O^T columns once the previous tile's MMAs are done (sound: the wait
+          // on pt_free at the top of this tile established that tile it-2's were)
           if (!mbar_wait(o_done, (it - 1) & 1)) alive = false;
           tc_fence_after();
 #pragma unroll
@@ -651,7 +686,11 @@ __global__ void __launch_bounds__(448, 1)
     if (!alive && lane == 0) atomicOr(p.err, kDevErrTimeout);
 
     // ------------------------------------------------------------ epilogue
-    if (ntiles > 0 && alive && !mbar_wait(o_done, (ntiles - 1) & 1)) alive = false;
+    // All MMAs done. (Not a wait on o_done for the last tile: a parity wait for phase k is
+    // only sound once phase k-1 has completed, and nothing here orders the PV MMAs of tile
+    // ntiles-2 before this point. pt_free of the last tile's buffer is sound -- this thread
+    // saw its previous phase, of tile ntiles-3 -- and its commit covers every earlier MMA.)
+    if (ntiles > 0 && alive && !mbar_wait(&pt_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) alive = false;
     tc_fence_after();
     // row sums over the 128 keys
 #pragma unroll
