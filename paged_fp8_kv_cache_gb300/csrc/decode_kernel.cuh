@@ -482,8 +482,9 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
 #pragma unroll
       for (int e = 0; e < 2; ++e) l_run[nt][e] += __shfl_xor_sync(0xffffffffu, l_run[nt][e], off);
 
-  // all consumers are done with the stage ring before it is reused
-  asm volatile("bar.sync 1, %0;" ::"r"(ncw * 32) : "memory");
+  // all consumers are done with the stage ring before it is reused (non-aligned form: a warp
+  // counts once, after all of its threads have arrived)
+  asm volatile("barrier.sync 1, %0;" ::"r"(ncw * 32) : "memory");
 
   float* obuf = reinterpret_cast<float*>(smem);  // [ncw][ROWS_W][D]
   float* my_o = obuf + static_cast<size_t>(warp) * ROWS_W * D;
@@ -505,7 +506,7 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
         *reinterpret_cast<float2*>(rowp + d0) = make_float2(o[i][nt][e], o[i][nt][2 + e]);
       }
   }
-  asm volatile("bar.sync 1, %0;" ::"r"(ncw * 32) : "memory");
+  asm volatile("barrier.sync 1, %0;" ::"r"(ncw * 32) : "memory");
 
   // each consumer thread finishes (row, 4 consecutive dims) items
   const int rows_cta = min(R, p.nrg * ROWS_W);

@@ -5,33 +5,40 @@
 // exact grouped q8 verification over FP8 KV) form a real dense tile.
 //
 // One CTA = one (key range, KV head, sequence), 14 warps:
-//   warp 0      producer: TMA tile copies of 128-key FP8 K/V tiles into a
-//               shared-memory ring (same tensor maps as the decode kernel);
+//   warp 0      producer: TMA tile copies of 128-key FP8 K and V tiles into
+//               two shared-memory rings (same tensor maps as the decode kernel);
 //   warp 1      MMA issuer (one lane) and TMEM owner;
-//   warps 2-5   K converter: each thread owns one TMEM lane = one key of the
-//               tile and turns its K row (FP8 -> fp16, exact) into the A
-//               operand of S^T = K Q^T, written with tcgen05.st;
-//   warps 6-9   softmax: each thread owns one key of the tile; it reads the
-//               key's logits for all rows from TMEM, masks, exponentiates
-//               against a per-row reference maximum and writes P^T (fp16)
-//               into a swizzled shared-memory B operand; at the end it reads
-//               O^T back from TMEM and writes the output;
+//   warps 2-9   softmax: each thread owns one key of the tile (its TMEM lane)
+//               and half of the query rows; it reads the key's logits from
+//               TMEM, masks, exponentiates against a per-row reference maximum
+//               and writes P^T (fp16) into a swizzled shared-memory B operand;
+//               at the end it reads O^T back from TMEM and writes the output;
 //   warps 10-13 V converter: each thread owns one TMEM lane = one or two
-//               head-dim elements and writes them for all keys of the tile
-//               as the A operand of O^T = V^T P^T.
-// MMAs: M = 128 (keys for S^T, head-dim elements for O^T), N = rows padded
-// to a multiple of 16, K = 16 per instruction, f16 inputs, f32 accumulators
-// in TMEM. Online softmax: every row keeps a reference maximum m; p is formed
-// against it in one pass. A tile whose logits exceed m by more than
-// kRescaleLog2 triggers an exact update (the tile's true row maxima are
-// reduced across the 128 keys; the running sums and the O^T accumulators are
-// rescaled and the tile is redone against the new references); the first
-// tile always does. Every wait is an mbarrier wait with a poll limit, so
-// every path of every role ends, and TMEM is freed after a CTA-wide barrier.
+//               head-dim elements and writes them for all keys of the tile,
+//               FP8 -> fp16 (exact), as the A operand of O^T = V^T P^T
+//               (two TMEM buffers, so tile i+1 is converted while the MMAs of
+//               tile i run).
+// S^T = K Q^T runs on FP8 directly (tcgen05.mma kind::f8f6f4, M = 128 keys):
+// the K tile is the A operand exactly as TMA left it in shared memory, and Q
+// is the sum of three E4M3 terms per element (row r scaled by 2^e_r so that
+// its largest element is at most 448; the terms are the successive
+// round-to-nearest residuals, so their sum is the fp16 Q element to within
+// half an E4M3 subnormal step). The three term MMAs accumulate into one f32
+// accumulator. O^T = V^T P^T runs on kind::f16 (M = 128 head-dim elements).
+// N = query rows padded to 32/48/64.
+// Online softmax: every row keeps a reference maximum m; p is formed against
+// it in one pass. A tile whose logits exceed m by more than kRescaleLog2
+// triggers an exact update (the tile's row maxima are reduced across the 128
+// keys, its first-pass terms are taken back out of the fp32 row sums, the
+// sums and the O^T accumulators are rescaled and the tile is redone); the
+// first tile goes straight to the update. Every wait is an mbarrier wait
+// with a time limit, so every path of every role ends; TMEM is freed by the
+// MMA warp once the softmax warps, its last readers, have signalled.
 #pragma once
 
 #include <cuda.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <math_constants.h>
 #include <stdint.h>
 
@@ -42,6 +49,8 @@
 namespace pfkv {
 
 constexpr float kRescaleLog2 = 8.f;
+constexpr int kQTerms = 3;
+constexpr int kSoftmaxWarps = 8;
 
 template <int D, int NMAX_>
 struct VerifyShape {
@@ -50,25 +59,26 @@ struct VerifyShape {
   static constexpr int SUB = KT * kBoxBytes;             // one box column of a tile (16 KB)
   static constexpr int KV_TILE = NBOX * SUB;             // K (or V) bytes per tile
   static constexpr int NMAX = NMAX_;                     // padded query rows (MMA N): 32, 48 or 64
-  static constexpr int Q_BYTES = (D / 64) * NMAX * 128;  // Q as K-major 128B-swizzled blocks of 64 dims
-  static constexpr int PT_BYTES = (KT / 64) * NMAX * 128;  // one P^T buffer (K-major, 64-key blocks)
+  static constexpr int HN = NMAX / 2;                    // rows per softmax warp
+  static constexpr int QT_BYTES = NBOX * NMAX * 128;     // one E4M3 term of Q: D/128 blocks of NMAX x 128 B
+  static constexpr int Q_BYTES = kQTerms * QT_BYTES;
+  static constexpr int PT_BYTES = (KT / 64) * NMAX * 128;  // one P^T buffer (fp16, K-major, 64-key blocks)
   static constexpr int MT = D / 128;                     // O^T M-tiles
   static constexpr int TMEM_COLS = 512;
   static constexpr int COL_S = 0;                        // 2 x NMAX: S^T double buffer
   static constexpr int COL_O = 2 * NMAX;                 // MT x NMAX: O^T
-  static constexpr int COL_AK = ((COL_O + MT * NMAX + 31) / 32) * 32;  // D/2: K as A operand (fp16 pairs)
-  static constexpr int COL_AV = COL_AK + D / 2;          // MT x KT/2: V^T as A operand
-  static_assert(COL_AV + MT * KT / 2 <= TMEM_COLS, "TMEM budget");
-  // misc: m_ref, alpha, wred[4], lsum[4], m_prev (NMAX floats each), flags, TMEM slot, barriers
-  static constexpr int MISC_BYTES = 11 * NMAX * 4 + 64 + 32 * 8;
-  // Separate K and V rings. V tiles are held longest (the V operand of tile i+1 can only be
-  // written once the PV MMAs of tile i are done), so the V ring gets whatever depth the
-  // remaining shared memory allows (2..4 tiles).
+  static constexpr int COL_AV = ((COL_O + MT * NMAX + 31) / 32) * 32;  // 2 x AV_COLS: V^T operands
+  static constexpr int AV_COLS = MT * KT / 2;            // one V^T operand (fp16 pairs)
+  static_assert(COL_AV + 2 * AV_COLS <= TMEM_COLS, "TMEM budget");
+  static_assert(HN % 8 == 0, "softmax rows come in TMEM loads of 8 columns");
+  // misc: m_ref, alpha, sc2r, rscale, wred[4], lsum[4] (NMAX floats each), out_row (NMAX ints),
+  // vote flags, TMEM slot, barriers
+  static constexpr int MISC_BYTES = 13 * NMAX * 4 + 64 + 32 * 8;
   static constexpr int kSmemLimit = 227 * 1024;
-  static constexpr int NK = KV_TILE <= 16384 ? 3 : 2;
-  static constexpr int NV_FIT = (kSmemLimit - 1024 - NK * KV_TILE - Q_BYTES - 2 * PT_BYTES - MISC_BYTES) / KV_TILE;
-  static constexpr int NV = NV_FIT > 4 ? 4 : NV_FIT;
-  static_assert(NV >= 2, "shared memory budget");
+  static constexpr int FIT = (kSmemLimit - 1024 - Q_BYTES - 2 * PT_BYTES - MISC_BYTES) / KV_TILE;
+  static constexpr int NK = FIT / 2 > 4 ? 4 : FIT / 2;
+  static constexpr int NV = FIT - NK > 4 ? 4 : FIT - NK;
+  static_assert(NK >= 2 && NV >= 2, "shared memory budget");
   // shared memory map (offsets from the 1 KB-aligned base)
   static constexpr int OFF_KRING = 0;
   static constexpr int OFF_VRING = OFF_KRING + NK * KV_TILE;
@@ -94,13 +104,28 @@ __device__ __forceinline__ uint32_t umma_idesc_f16(int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
 }
 
-// D (TMEM) (+)= A (TMEM) * B (shared memory)
+// M = 128, N = n, A: FP8 codes (afmt 0 = E4M3, 1 = E5M2), B: E4M3, f32 accumulators, both K-major.
+__device__ __forceinline__ uint32_t umma_idesc_f8(int n, uint32_t afmt) {
+  return (1u << 4) | (afmt << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
+// D (TMEM) (+)= A (TMEM) * B (shared memory), f16 operands
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                         uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
+// D (TMEM) (+)= A (shared memory) * B (shared memory), FP8 operands
+__device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -120,13 +145,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
-        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-      : "r"(taddr)
-      : "memory");
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "r"(taddr)
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -147,12 +176,38 @@ __device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t two) {
   }
 }
 
+// Exponent e with 2^e * mx <= 448 (the largest E4M3 value, 1.75 * 2^8) and 2^(e+1) * mx > 448,
+// for a finite mx > 0; 0 otherwise. Exact: read off the bits of mx.
+__device__ __forceinline__ int e4m3_row_exponent(float mx) {
+  const uint32_t u = __float_as_uint(mx);
+  const int be = static_cast<int>((u >> 23) & 0xFF);
+  if (!(mx > 0.f) || be == 0xFF) return 0;
+  if (be == 0) return 0;  // below the fp32 normal range: cannot come from an fp16 input
+  const int E = be - 127;
+  const uint32_t frac = u & 0x7FFFFF;  // mantissa bits of 1.f
+  return (frac <= 0x600000u) ? 8 - E : 7 - E;  // 1.f <= 1.75 ?
+}
+
+// x0, x1 (exactly representable sums of at most three E4M3 values once scaled) as three
+// successive round-to-nearest E4M3 residual terms; term k of the pair in the low/high byte of t[k].
+__device__ __forceinline__ void split3_e4m3(float x0, float x1, uint32_t (&t)[kQTerms]) {
+#pragma unroll
+  for (int k = 0; k < kQTerms; ++k) {
+    const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+    t[k] = c;
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(c, __NV_E4M3);
+    const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+    x0 -= back.x;  // exact: the residual is a multiple of the input's quantum
+    x1 -= back.y;
+  }
+}
+
 template <int D, int KV, int NMAX_>
 __global__ void __launch_bounds__(448, 1)
     verify_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeParams p) {
   using S = VerifyShape<D, NMAX_>;
-  constexpr int KT = S::KT, NBOX = S::NBOX, NK = S::NK, NV = S::NV, NMAX = S::NMAX, MT = S::MT;
+  constexpr int KT = S::KT, NBOX = S::NBOX, NK = S::NK, NV = S::NV, NMAX = S::NMAX, MT = S::MT, HN = S::HN;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -178,25 +233,26 @@ __global__ void __launch_bounds__(448, 1)
 
   float* m_ref = reinterpret_cast<float*>(smem + S::OFF_MISC);  // [NMAX] reference max (log2 units)
   float* alpha_s = m_ref + NMAX;                                 // [NMAX] rescale factors
-  float* wred = alpha_s + NMAX;                                  // [4][NMAX] per-warp maxima
-  float* lsum = wred + 4 * NMAX;                                 // [4][NMAX] per-warp row sums
-  float* m_prev = lsum + 4 * NMAX;                               // [NMAX] references before an update
-  int* flag = reinterpret_cast<int*>(m_prev + NMAX);             // [3] rescale votes
+  float* sc2r = alpha_s + NMAX;                                  // [NMAX] logit scale of row r (log2 units)
+  float* rscale = sc2r + NMAX;                                   // [NMAX] output scale v_scale / L
+  float* wred = rscale + NMAX;                                   // [4][NMAX] per-quadrant maxima
+  float* lsum = wred + 4 * NMAX;                                 // [4][NMAX] per-quadrant row sums
+  int* out_row = reinterpret_cast<int*>(lsum + 4 * NMAX);        // [NMAX] output row of row r
+  int* flag = out_row + NMAX;                                    // [3] rescale votes
   uint32_t* tslot = reinterpret_cast<uint32_t*>(flag + 4);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_MISC + 11 * NMAX * 4 + 64);
-  uint64_t* kfull = bars;              // [NK] producer -> K converter
-  uint64_t* kempty = kfull + NK;       // [NK] K converter -> producer
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_MISC + 13 * NMAX * 4 + 64);
+  uint64_t* kfull = bars;              // [NK] producer -> MMA (K tile landed)
+  uint64_t* kempty = kfull + NK;       // [NK] MMA commit: S^T MMAs done reading the K tile
   uint64_t* vfull = kempty + NK;       // [NV] producer -> V converter
   uint64_t* vempty = vfull + NV;       // [NV] V converter -> producer
-  uint64_t* ak_full = vempty + NV;     // K converter -> MMA (K operand written)
-  uint64_t* av_full = ak_full + 1;     // V converter -> MMA (V operand written)
-  uint64_t* ak_free = av_full + 1;     // MMA commit: S^T MMAs done with the K operand
-  uint64_t* s_full = ak_free + 1;      // [2] MMA commit: S^T ready
+  uint64_t* av_full = vempty + NV;     // [2] V converter -> MMA (V^T operand written)
+  uint64_t* av_free = av_full + 2;     // [2] MMA commit: O^T MMAs done with a V^T operand
+  uint64_t* s_full = av_free + 2;      // [2] MMA commit: S^T ready
   uint64_t* s_free = s_full + 2;       // [2] softmax -> MMA: S^T read
   uint64_t* pt_full = s_free + 2;      // [2] softmax -> MMA: P^T written
-  uint64_t* pt_free = pt_full + 2;     // [2] MMA commit: O^T MMAs done reading P^T buffer
-  uint64_t* o_done = pt_free + 2;      // MMA commit: O^T MMAs of a tile done
-  uint64_t* swg_bar = o_done + 1;      // softmax warpgroup rendezvous (bounded waits, unlike bar.sync)
+  uint64_t* pt_free = pt_full + 2;     // [2] MMA commit: O^T MMAs of the tile done (P^T buffer free)
+  uint64_t* swg_bar = pt_free + 2;     // softmax warps' rendezvous (bounded waits, unlike bar.sync)
+  uint64_t* tmem_done = swg_bar + 1;   // softmax warps -> MMA warp: last TMEM read done
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
@@ -204,23 +260,22 @@ __global__ void __launch_bounds__(448, 1)
   if (tid == 0) {
     for (int s = 0; s < NK; ++s) {
       mbar_init(&kfull[s], 1);
-      mbar_init(&kempty[s], 4);  // one arrival per K-converter warp
+      mbar_init(&kempty[s], 1);
     }
     for (int s = 0; s < NV; ++s) {
       mbar_init(&vfull[s], 1);
       mbar_init(&vempty[s], 4);  // one arrival per V-converter warp
     }
-    mbar_init(ak_full, 4);
-    mbar_init(av_full, 4);
-    mbar_init(ak_free, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&av_full[i], 4);
+      mbar_init(&av_free[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
-      mbar_init(&pt_full[i], 4);
+      mbar_init(&s_free[i], kSoftmaxWarps);
+      mbar_init(&pt_full[i], kSoftmaxWarps);
       mbar_init(&pt_free[i], 1);
     }
-    mbar_init(o_done, 1);
-    mbar_init(swg_bar, 4);
+    mbar_init(swg_bar, kSoftmaxWarps);
+    mbar_init(tmem_done, kSoftmaxWarps);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -228,18 +283,68 @@ __global__ void __launch_bounds__(448, 1)
                  "r"(S::TMEM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  // Q -> shared memory (K-major, 128B swizzle), padded rows zero; softmax state
+  const float kscale = *p.k_scale, vscale = *p.v_scale;
+  const float sc2 = p.softmax_scale * kscale * 1.4426950408889634f;
+  // Q -> three E4M3 terms in shared memory (K-major, 128B swizzle), one warp per row; padded rows zero
   {
-    unsigned char* sq = smem + S::OFF_Q;
-    for (int idx = tid; idx < NMAX * (D / 8); idx += blockDim.x) {
-      const int r = idx / (D / 8);
-      const int d8 = (idx - r * (D / 8)) * 8;  // 8 consecutive dims = one 16-byte chunk
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    constexpr int PER_LANE = D / 32;  // 8 (D = 256) or 4 (D = 128) consecutive dims per lane
+    for (int r = warp; r < NP; r += 14) {
+      float x[PER_LANE];
+      float mx = 0.f;
       if (r < R) {
         const int t = r / p.G, j = r - t * p.G;
-        v = *reinterpret_cast<const uint4*>(p.q + ((static_cast<size_t>(b) * p.T + t) * p.num_q_heads + kvh * p.G + j) * D + d8);
+        const __half* src = p.q + ((static_cast<size_t>(b) * p.T + t) * p.num_q_heads + kvh * p.G + j) * D + lane * PER_LANE;
+        if constexpr (PER_LANE == 8) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            x[2 * i] = f.x;
+            x[2 * i + 1] = f.y;
+          }
+        } else {
+          const uint2 v = *reinterpret_cast<const uint2*>(src);
+          const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            x[2 * i] = f.x;
+            x[2 * i + 1] = f.y;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) mx = fmaxf(mx, fabsf(x[i]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i) x[i] = 0.f;
       }
-      *reinterpret_cast<uint4*>(sq + (d8 >> 6) * NMAX * 128 + sw128_elem(r, d8 & 63)) = v;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const int e = e4m3_row_exponent(mx);
+      const float up = __int_as_float((127 + e) << 23);    // 2^e (e in [-8, 32] for fp16 rows)
+      const float down = __int_as_float((127 - e) << 23);  // 2^-e
+      if (lane == 0) sc2r[r] = sc2 * down;
+      uint32_t tw[kQTerms][PER_LANE / 4];  // per term: PER_LANE codes as 32-bit words
+#pragma unroll
+      for (int i = 0; i < PER_LANE; i += 4) {
+        uint32_t lo[kQTerms], hi[kQTerms];
+        split3_e4m3(x[i] * up, x[i + 1] * up, lo);
+        split3_e4m3(x[i + 2] * up, x[i + 3] * up, hi);
+#pragma unroll
+        for (int k = 0; k < kQTerms; ++k) tw[k][i / 4] = (lo[k] & 0xFFFFu) | (hi[k] << 16);
+      }
+      const int d0 = lane * PER_LANE;
+      const int off = (d0 >> 7) * NMAX * 128 + r * 128 + (((((d0 & 127) >> 4) ^ r) & 7) << 4) + (d0 & 15);
+#pragma unroll
+      for (int k = 0; k < kQTerms; ++k) {
+        unsigned char* dst = smem + S::OFF_Q + k * S::QT_BYTES + off;
+        if constexpr (PER_LANE == 8) {
+          *reinterpret_cast<uint2*>(dst) = make_uint2(tw[k][0], tw[k][1]);
+        } else {
+          *reinterpret_cast<uint32_t*>(dst) = tw[k][0];
+        }
+      }
     }
     for (int i = tid; i < NMAX; i += blockDim.x) m_ref[i] = -CUDART_INF_F;
     if (tid == 0) flag[0] = flag[1] = flag[2] = 0;
@@ -249,9 +354,6 @@ __global__ void __launch_bounds__(448, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-
-  const float kscale = *p.k_scale, vscale = *p.v_scale;
-  const float sc2 = p.softmax_scale * kscale * 1.4426950408889634f;
   bool alive = true;
 
   if (warp == 0) {
@@ -282,7 +384,6 @@ __global__ void __launch_bounds__(448, 1)
         }
         return __shfl_sync(0xffffffffu, my_id, pidx - chunk_base);
       };
-      // rows of the tile's 64-row boxes (P >= 64) or pages (P < 64); at most 8
       auto wait_slot = [&](uint64_t* bar, int it, int depth) -> bool {
         if (it < depth) return true;
         bool got = true;
@@ -292,15 +393,17 @@ __global__ void __launch_bounds__(448, 1)
       for (int it = 0; it < ntiles && alive; ++it) {
         const int tile_start = t0 + it * KT;
         const int valid = min(KT, t1 - tile_start);
+        // rows of the tile's 64-row boxes (P >= 64) or pages (P < 64); at most 8
         int rows[8], box_rows, nbox_rows;
         if (P >= kTileKeys) {
           nbox_rows = (valid + kTileKeys - 1) / kTileKeys;
           box_rows = kTileKeys;
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
+          for (int hf = 0; hf < 8; ++hf) {
             const int key = tile_start + hf * kTileKeys;
             rows[hf] = 0;
-            if (hf < nbox_rows) rows[hf] = (page_id(key >> p.page_shift) * p.num_kv_heads + kvh) * P + (key & (P - 1));
+            if (hf < 2 && hf < nbox_rows)
+              rows[hf] = (page_id(key >> p.page_shift) * p.num_kv_heads + kvh) * P + (key & (P - 1));
           }
         } else {
           nbox_rows = (valid + P - 1) >> p.page_shift;
@@ -327,11 +430,14 @@ __global__ void __launch_bounds__(448, 1)
           const CUtensorMap* map = which == 0 ? &tmk : &tmv;
           if (lane == 0) {
             mbar_arrive_expect_tx(&fullb[it % depth], bytes);
-            for (int r = 0; r < nbox_rows; ++r) {
 #pragma unroll
-              for (int bx = 0; bx < NBOX; ++bx)
-                tma_load_2d(dst + bx * S::SUB + r * box_rows * kBoxBytes, map, &fullb[it % depth], bx * kBoxBytes,
-                            rows[r]);
+            for (int r = 0; r < 8; ++r) {
+              if (r < nbox_rows) {
+#pragma unroll
+                for (int bx = 0; bx < NBOX; ++bx)
+                  tma_load_2d(dst + bx * S::SUB + r * box_rows * kBoxBytes, map, &fullb[it % depth], bx * kBoxBytes,
+                              rows[r]);
+              }
             }
           }
         }
@@ -354,45 +460,53 @@ __global__ void __launch_bounds__(448, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && ntiles > 0) {
-      const uint32_t idesc = umma_idesc_f16(NP);
+      const uint32_t idesc_qk = umma_idesc_f8(NP, KV == kKvE4m3 ? 0u : 1u);
+      const uint32_t idesc_pv = umma_idesc_f16(NP);
       const uint32_t q_base = smem_u32(smem + S::OFF_Q);
+      const uint32_t k_base = smem_u32(smem + S::OFF_KRING);
       const uint32_t pt_base = smem_u32(smem + S::OFF_PT);
-      // Issue whichever MMA group is ready: S^T of the next tile (its K operand written, its
-      // S buffer released by the softmax) or O^T of the oldest tile whose V operand and P^T
+      // Issue whichever MMA group is ready: S^T of the next tile (its K tile landed, its S
+      // buffer released by the softmax) or O^T of the oldest tile whose V^T operand and P^T
       // are written. Neither waits behind the other.
       int sn = 0, on = 0;
       bool ok = true;
       uint64_t last = global_ns();
       while (on < ntiles) {
         bool progress = false;
-        if (sn < ntiles && mbar_test(ak_full, sn & 1) &&
+        if (sn < ntiles && mbar_test(&kfull[sn % NK], (sn / NK) & 1) &&
             (sn < 2 || mbar_test(&s_free[sn & 1], ((sn >> 1) - 1) & 1))) {
           tc_fence_after();
           const uint32_t d_t = tbase + S::COL_S + (sn & 1) * NMAX;
+          const uint32_t ka = k_base + (sn % NK) * S::KV_TILE;
 #pragma unroll 1
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t bd = umma_desc_sw128(q_base + (ks >> 2) * NMAX * 128 + (ks & 3) * 32);
-            umma_ts(d_t, tbase + S::COL_AK + 8 * ks, bd, idesc, ks > 0 ? 1u : 0u);
+          for (int ks = 0; ks < D / 32; ++ks) {  // 32 FP8 dims = 32 bytes of a swizzled row per MMA
+            const uint64_t ad = umma_desc_sw128(ka + (ks >> 2) * S::SUB + (ks & 3) * 32);
+#pragma unroll
+            for (int k = 0; k < kQTerms; ++k) {
+              const uint64_t bd = umma_desc_sw128(q_base + k * S::QT_BYTES + (ks >> 2) * NMAX * 128 + (ks & 3) * 32);
+              umma_ss_f8(d_t, ad, bd, idesc_qk, (ks > 0 || k > 0) ? 1u : 0u);
+            }
           }
           umma_commit(&s_full[sn & 1]);
-          umma_commit(ak_free);
+          umma_commit(&kempty[sn % NK]);
           ++sn;
           progress = true;
         }
-        if (on < sn && mbar_test(av_full, on & 1) && mbar_test(&pt_full[on & 1], (on >> 1) & 1)) {
+        if (on < sn && mbar_test(&av_full[on & 1], (on >> 1) & 1) && mbar_test(&pt_full[on & 1], (on >> 1) & 1)) {
           tc_fence_after();
           const uint32_t pt = pt_base + (on & 1) * S::PT_BYTES;
+          const uint32_t av = tbase + S::COL_AV + (on & 1) * S::AV_COLS;
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll 1
             for (int ks = 0; ks < KT / 16; ++ks) {
               const uint64_t bd = umma_desc_sw128(pt + (ks >> 2) * NMAX * 128 + (ks & 3) * 32);
-              umma_ts(tbase + S::COL_O + mt * NMAX, tbase + S::COL_AV + mt * (KT / 2) + 8 * ks, bd, idesc,
+              umma_ts(tbase + S::COL_O + mt * NMAX, av + mt * (KT / 2) + 8 * ks, bd, idesc_pv,
                       (on > 0 || ks > 0) ? 1u : 0u);
             }
           }
           umma_commit(&pt_free[on & 1]);
-          umma_commit(o_done);
+          umma_commit(&av_free[on & 1]);
           ++on;
           progress = true;
         }
@@ -409,46 +523,6 @@ __global__ void __launch_bounds__(448, 1)
       if (!ok) atomicOr(p.err, kDevErrTimeout);
     }
     __syncwarp();
-  } else if (warp < 6) {
-    // ---------------------------------------------------------------- K converter (warps 2-5)
-    const int q = warp & 3;              // TMEM lane quadrant of this warp
-    const int key_row = 32 * q + lane;   // this thread's key of the tile = its TMEM lane
-    const uint32_t tq = tbase + (static_cast<uint32_t>(32 * q) << 16);
-    for (int it = 0; it < ntiles; ++it) {
-      const int s = it % NK;
-      if (!mbar_wait(&kfull[s], (it / NK) & 1) || (it > 0 && !mbar_wait(ak_free, (it - 1) & 1))) {
-        alive = false;
-        break;
-      }
-      tc_fence_after();
-      const unsigned char* Ks = smem + S::OFF_KRING + s * S::KV_TILE;
-#pragma unroll
-      for (int bx = 0; bx < NBOX; ++bx) {
-#pragma unroll
-        for (int cp = 0; cp < 4; ++cp) {  // two 16-byte chunks = 32 codes = 16 fp16 pairs = 16 columns
-          uint32_t u[16];
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const uint4 v = lds128(Ks + bx * S::SUB + swz_offset(key_row, 2 * cp + cc));
-            const uint32_t x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              u[cc * 8 + 2 * j] = fp8x2_to_f16x2<KV>(x[j]);            // dims 4j, 4j+1 of the chunk
-              u[cc * 8 + 2 * j + 1] = fp8x2_to_f16x2<KV>(x[j] >> 16);  // dims 4j+2, 4j+3
-            }
-          }
-          tmem_st16(tq + S::COL_AK + bx * 64 + cp * 16, u);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(ak_full);
-        mbar_arrive(&kempty[s]);
-      }
-    }
-    if (!alive && lane == 0) atomicOr(p.err, kDevErrTimeout);
   } else if (warp >= 10) {
     // ---------------------------------------------------------------- V converter (warps 10-13)
     // TMEM lane L of O^T M-tile mt holds head-dim element 2L + mt (D = 256) or L (D = 128);
@@ -464,12 +538,15 @@ __global__ void __launch_bounds__(448, 1)
     for (int j = 0; j < 8; ++j) voff[j] = vbx * S::SUB + swz_offset(j, vbyte >> 4) + (vbyte & 15);
     for (int it = 0; it < ntiles; ++it) {
       const int s = it % NV;
-      if (!mbar_wait(&vfull[s], (it / NV) & 1) || (it > 0 && !mbar_wait(o_done, (it - 1) & 1))) {
+      // V^T buffer it&1 is free once the O^T MMAs of tile it-2 are done (sound: this thread
+      // saw that barrier's previous phase, of tile it-4, before converting tile it-2)
+      if (!mbar_wait(&vfull[s], (it / NV) & 1) || (it >= 2 && !mbar_wait(&av_free[it & 1], ((it >> 1) - 1) & 1))) {
         alive = false;
         break;
       }
       tc_fence_after();
       const unsigned char* Vs = smem + S::OFF_VRING + s * S::KV_TILE;
+      const uint32_t av = tq + S::COL_AV + (it & 1) * S::AV_COLS;
       const int valid = min(KT, t1 - (t0 + it * KT));
       const bool tail = valid < KT;
 #pragma unroll 1
@@ -496,36 +573,55 @@ __global__ void __launch_bounds__(448, 1)
           v0[kk >> 1] = fp8x2_to_f16x2<KV>(X);
           v1[kk >> 1] = fp8x2_to_f16x2<KV>(X >> 16);
         }
-        tmem_st16(tq + S::COL_AV + (k0 >> 1), v0);
-        if constexpr (MT == 2) tmem_st16(tq + S::COL_AV + KT / 2 + (k0 >> 1), v1);
+        tmem_st16(av + (k0 >> 1), v0);
+        if constexpr (MT == 2) tmem_st16(av + KT / 2 + (k0 >> 1), v1);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(av_full);
+        mbar_arrive(&av_full[it & 1]);
         mbar_arrive(&vempty[s]);
       }
     }
     if (!alive && lane == 0) atomicOr(p.err, kDevErrTimeout);
   } else {
-    // ---------------------------------------------------------------- softmax + epilogue (warps 6-9)
-    const int q = warp & 3;
-    const int sw = warp - 6;  // 0..3 within the softmax warpgroup
+    // ---------------------------------------------------------------- softmax + epilogue (warps 2-9)
+    const int sw = warp - 2;           // 0..7 within the softmax warps
+    const int q = warp & 3;            // TMEM lane quadrant
+    const int rbase = (sw >> 2) * HN;  // this warp's rows: rbase .. rbase + HN - 1
     const int key_lane = 32 * q + lane;
+    const int sidx = sw * 32 + lane;   // 0..255: the row owned in the per-row steps
     const uint32_t tq = tbase + (static_cast<uint32_t>(32 * q) << 16);
     uint32_t swg_phase = 0;
-    // the 4 softmax warps meet; a wait that runs out marks the CTA's work as failed
+    // the softmax warps meet; a wait that runs out marks the CTA's work as failed
     auto swg_sync = [&]() {
       __syncwarp();
       if (lane == 0) mbar_arrive(swg_bar);
       if (!mbar_wait(swg_bar, swg_phase & 1)) alive = false;
       ++swg_phase;
     };
-    float l_part[NMAX];  // this thread's (key lane's) share of every row sum, fp32
+    float l_part[HN];  // this thread's (key lane's) share of its rows' sums, fp32
 #pragma unroll
-    for (int r = 0; r < NMAX; ++r) l_part[r] = 0.f;
+    for (int r = 0; r < HN; ++r) l_part[r] = 0.f;
     const int tlim_base = N - p.T;  // row r sees keys <= N - T + r / G
+    auto load8 = [](const float* src, float (&m)[8]) {
+      const float4 a = *reinterpret_cast<const float4*>(src);
+      const float4 c = *reinterpret_cast<const float4*>(src + 4);
+      m[0] = a.x;
+      m[1] = a.y;
+      m[2] = a.z;
+      m[3] = a.w;
+      m[4] = c.x;
+      m[5] = c.y;
+      m[6] = c.z;
+      m[7] = c.w;
+    };
+    // 2^(s - m) against a reference m; 0 while a row has no reference yet, and capped so
+    // that a logit that outgrew its reference (the tile is then redone) stays finite
+    auto pexp = [](float s2, float m) -> float {
+      return m == -CUDART_INF_F ? 0.f : fast_exp2(fminf(s2 - m, 15.f));
+    };
     for (int it = 0; it < ntiles && alive; ++it) {
       const int sb = it & 1;
       if (!mbar_wait(&s_full[sb], (it >> 1) & 1)) {
@@ -533,148 +629,121 @@ __global__ void __launch_bounds__(448, 1)
         break;
       }
       tc_fence_after();
-      // P^T buffer sb is free once the O^T MMAs of tile it-2 are done (its own barrier:
-      // o_done may already be a phase further, which a parity wait cannot tell apart)
+      // P^T buffer sb is free once the O^T MMAs of tile it-2 are done
       if (it >= 2 && !mbar_wait(&pt_free[sb], ((it >> 1) - 1) & 1)) {
         alive = false;
         break;
       }
-      const uint32_t s_col = tq + S::COL_S + sb * NMAX;
+      const uint32_t s_col = tq + S::COL_S + sb * NMAX + rbase;
       const int tile_start = t0 + it * KT;
       const int kp = tile_start + key_lane;  // absolute key position
       const bool in_range = kp < t1;
       // row r sees this key iff r / G >= kp - (N - T), i.e. r >= G * (kp - (N - T))
       const int rmin = p.G * (kp - tlim_base);
       const bool all_vis = (tile_start + KT <= t1) && (tile_start + KT - 1 <= tlim_base);  // CTA-uniform
-      // logits of 16 rows (columns c0..c0+15) of this thread's key, scaled to base 2 and masked
-      auto load_s2 = [&](int c0, float (&s2)[16]) {
-        uint32_t v[16];
-        tmem_ld16(s_col + c0, v);
+      // logits of rows rbase+c .. rbase+c+7 of this thread's key, in base-2 units, masked
+      auto load_s2 = [&](int c, float (&s2)[8]) {
+        uint32_t v[8];
+        float sc[8];
+        tmem_ld8(s_col + c, v);
+        load8(sc2r + rbase + c, sc);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r = c0 + j;
+        for (int j = 0; j < 8; ++j) {
+          const int r = rbase + c + j;
           const bool vis = all_vis || (in_range && (r >= R || r >= rmin));
-          s2[j] = vis ? __uint_as_float(v[j]) * sc2 : -CUDART_INF_F;
+          s2[j] = vis ? __uint_as_float(v[j]) * sc[j] : -CUDART_INF_F;
         }
-      };
-      auto load_m = [&](const float* src, int c0, float (&m)[16]) {
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float4 mv = *reinterpret_cast<const float4*>(src + c0 + 4 * q4);
-          m[4 * q4] = mv.x;
-          m[4 * q4 + 1] = mv.y;
-          m[4 * q4 + 2] = mv.z;
-          m[4 * q4 + 3] = mv.w;
-        }
-      };
-      // 2^(s - m) against a reference m; 0 while a row has no reference yet, and capped so
-      // that a logit that outgrew its reference (the tile is then redone) stays finite
-      auto pexp = [](float s2, float m) -> float {
-        return m == -CUDART_INF_F ? 0.f : fast_exp2(fminf(s2 - m, 15.f));
       };
       unsigned char* pt = smem + S::OFF_PT + sb * S::PT_BYTES + (key_lane >> 6) * NMAX * 128;
       const int kk = key_lane & 63;
-      // one pass: P^T and the row sums against the current references; note outgrown rows
-      bool exceed = false;
+      bool update = (it == 0);  // the first tile has no references yet
+      bool did_pass = false;
+#pragma unroll 1
+      for (int round = 0; round < 2; ++round) {
+        if (update) {
+          // exact update: this tile's row maxima over its 128 keys; this tile's first-pass
+          // terms (same formula, same values) taken back out of the row sums
 #pragma unroll
-      for (int c0 = 0; c0 < NMAX; c0 += 16) {
-        if (c0 < NP) {
-          float s2[16], m[16];
-          load_s2(c0, s2);
-          load_m(m_ref, c0, m);
+          for (int c = 0; c < HN; c += 8) {
+            float s2[8], m[8];
+            load_s2(c, s2);
+            load8(m_ref + rbase + c, m);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            exceed |= (s2[j] > m[j] + kRescaleLog2);
-            const float pr = pexp(s2[j], m[j]);
-            l_part[c0 + j] += pr;
-            *reinterpret_cast<__half*>(pt + sw128_elem(c0 + j, kk)) = __float2half_rn(pr);
-          }
-        }
-      }
-      // exact update of the reference maxima when any logit outgrew its row's
-      // (three rotating flags: the one cleared here, of tile it-1, was read by every
-      // thread before it reached this tile's rendezvous, and is voted on again only
-      // after the next rendezvous, which the clearing thread must reach first)
-      if (__any_sync(0xffffffffu, exceed) && lane == 0) atomicOr(&flag[it % 3], 1);
-      swg_sync();
-      const bool rescale = flag[it % 3] != 0;
-      if (threadIdx.x == 6 * 32) flag[(it + 2) % 3] = 0;
-      if (rescale) {
-#pragma unroll
-        for (int c0 = 0; c0 < NMAX; c0 += 16) {
-          if (c0 < NP) {
-            float s2[16];
-            load_s2(c0, s2);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < 8; ++j) {
               float mx = s2[j];
 #pragma unroll
               for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-              if (lane == 0) wred[sw * NMAX + c0 + j] = mx;
+              if (lane == 0) wred[q * NMAX + rbase + c + j] = mx;
+              if (did_pass) l_part[c + j] -= pexp(s2[j], m[j]);
             }
           }
-        }
-        swg_sync();
-        if (key_lane < NP) {
-          const int r = key_lane;
-          const float mt = fmaxf(fmaxf(wred[r], wred[NMAX + r]), fmaxf(wred[2 * NMAX + r], wred[3 * NMAX + r]));
-          const float mo = m_ref[r];
-          const float mn = fmaxf(mo, mt);
-          // the reference only moves up; rows with nothing visible so far keep -inf
-          alpha_s[r] = (mo == -CUDART_INF_F) ? 0.f : fast_exp2(mo - mn);
-          m_prev[r] = mo;
-          m_ref[r] = mn;
-        }
-        swg_sync();
-        // take this tile's first-pass terms back out (same formula, same values), rescale the
-        // earlier tiles' share, then redo the tile against the new references
-#pragma unroll
-        for (int c0 = 0; c0 < NMAX; c0 += 16) {
-          if (c0 < NP) {
-            float s2[16], m[16];
-            load_s2(c0, s2);
-            load_m(m_prev, c0, m);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) l_part[c0 + j] = (l_part[c0 + j] - pexp(s2[j], m[j])) * alpha_s[c0 + j];
+          swg_sync();
+          if (sidx < NP) {
+            const int r = sidx;
+            const float mt = fmaxf(fmaxf(wred[r], wred[NMAX + r]), fmaxf(wred[2 * NMAX + r], wred[3 * NMAX + r]));
+            const float mo = m_ref[r];
+            const float mn = fmaxf(mo, mt);
+            // the reference only moves up; rows with nothing visible so far keep -inf
+            alpha_s[r] = (mo == -CUDART_INF_F) ? 0.f : fast_exp2(mo - mn);
+            m_ref[r] = mn;
           }
-        }
-        if (it > 0) {
-          // rescale the O^T columns once the previous tile's MMAs are done (sound: the wait
-          // on pt_free at the top of this tile established that tile it-2's were)
-          if (!mbar_wait(o_done, (it - 1) & 1)) alive = false;
-          tc_fence_after();
+          swg_sync();
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
+          for (int c = 0; c < HN; c += 8) {
+            float a[8];
+            load8(alpha_s + rbase + c, a);
 #pragma unroll
-            for (int c0 = 0; c0 < NMAX; c0 += 16) {
-              if (c0 < NP) {
-                uint32_t v[16];
-                const uint32_t a = tq + S::COL_O + mt * NMAX + c0;
-                tmem_ld16(a, v);
+            for (int j = 0; j < 8; ++j) l_part[c + j] *= a[j];
+          }
+          if (it > 0) {
+            // rescale the O^T columns once the previous tile's MMAs are done (sound: this
+            // thread saw that barrier's previous phase, of tile it-3, at the top of tile it-1)
+            if (!mbar_wait(&pt_free[(it - 1) & 1], ((it - 1) >> 1) & 1)) alive = false;
+            tc_fence_after();
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+              for (int c = 0; c < HN; c += 8) {
+                uint32_t v[8];
+                float a[8];
+                const uint32_t addr = tq + S::COL_O + mt * NMAX + rbase + c;
+                tmem_ld8(addr, v);
+                load8(alpha_s + rbase + c, a);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha_s[c0 + j]);
-                tmem_st16(a, v);
+                for (int j = 0; j < 8; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * a[j]);
+                tmem_st8(addr, v);
               }
             }
-          }
-          tmem_wait_st();
-        }
-#pragma unroll
-        for (int c0 = 0; c0 < NMAX; c0 += 16) {
-          if (c0 < NP) {
-            float s2[16], m[16];
-            load_s2(c0, s2);
-            load_m(m_ref, c0, m);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float pr = pexp(s2[j], m[j]);
-              l_part[c0 + j] += pr;
-              *reinterpret_cast<__half*>(pt + sw128_elem(c0 + j, kk)) = __float2half_rn(pr);
-            }
+            tmem_wait_st();
           }
         }
+        // one pass: P^T and the row sums against the current references; note outgrown rows
+        bool exceed = false;
+#pragma unroll
+        for (int c = 0; c < HN; c += 8) {
+          float s2[8], m[8];
+          load_s2(c, s2);
+          load8(m_ref + rbase + c, m);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            exceed |= (s2[j] > m[j] + kRescaleLog2);
+            const float pr = pexp(s2[j], m[j]);
+            l_part[c + j] += pr;
+            *reinterpret_cast<__half*>(pt + sw128_elem(rbase + c + j, kk)) = __float2half_rn(pr);
+          }
+        }
+        did_pass = true;
+        if (update) break;  // after an update no logit exceeds its reference
+        // (three rotating flags: the one cleared here, of tile it-1, was read by every
+        // thread before it reached this tile's rendezvous, and is voted on again only
+        // after the next rendezvous, which the clearing thread must reach first)
+        if (__any_sync(0xffffffffu, exceed) && lane == 0) atomicOr(&flag[it % 3], 1);
+        swg_sync();
+        update = flag[it % 3] != 0;
+        if (sidx == 0) flag[(it + 2) % 3] = 0;
+        if (!update) break;
       }
       tc_fence_before();
       __syncwarp();
@@ -686,65 +755,94 @@ __global__ void __launch_bounds__(448, 1)
     if (!alive && lane == 0) atomicOr(p.err, kDevErrTimeout);
 
     // ------------------------------------------------------------ epilogue
-    // All MMAs done. (Not a wait on o_done for the last tile: a parity wait for phase k is
-    // only sound once phase k-1 has completed, and nothing here orders the PV MMAs of tile
-    // ntiles-2 before this point. pt_free of the last tile's buffer is sound -- this thread
-    // saw its previous phase, of tile ntiles-3 -- and its commit covers every earlier MMA.)
+    // All MMAs done: pt_free of the last tile's buffer (sound: this thread saw its previous
+    // phase, of tile ntiles-3) is committed after every earlier MMA.
     if (ntiles > 0 && alive && !mbar_wait(&pt_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) alive = false;
     tc_fence_after();
     // row sums over the 128 keys
 #pragma unroll
-    for (int r = 0; r < NMAX; ++r) {
-      float v = l_part[r];
+    for (int j = 0; j < HN; ++j) {
+      float v = l_part[j];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (lane == 0) lsum[sw * NMAX + r] = v;
+      if (lane == 0) lsum[q * NMAX + rbase + j] = v;
     }
     swg_sync();
     const bool final_out = (nsplit_b == 1);
-    // this thread's TMEM lane = head-dim element(s) of O^T
+    if (sidx < R) {  // per row: output scale, output row, LSE
+      const int r = sidx;
+      const float L = lsum[r] + lsum[NMAX + r] + lsum[2 * NMAX + r] + lsum[3 * NMAX + r];
+      const float M = m_ref[r];
+      const bool has = alive && ntiles > 0 && (M != -CUDART_INF_F) && (L > 0.f);
+      const int t = r / p.G, jj = r - t * p.G;
+      const int grow = (b * p.T + t) * p.num_q_heads + kvh * p.G + jj;
+      rscale[r] = has ? vscale / L : 0.f;
+      out_row[r] = grow;
+      const float lse_val = has ? (M + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
+      if (final_out) {
+        p.lse[grow] = lse_val;
+      } else {
+        p.lse_part[static_cast<size_t>(grow) * p.num_splits + split] = lse_val;
+      }
+    }
+    swg_sync();
+    // this thread's TMEM lane = head-dim element(s) of O^T; its rows: rbase .. rbase + HN - 1
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      const int d_out = (MT == 2) ? 2 * key_lane + mt : key_lane;
+    for (int c = 0; c < HN; c += 8) {
+      if (rbase + c >= R) break;
+      uint32_t v[MT][8];
 #pragma unroll
-      for (int c0 = 0; c0 < NMAX; c0 += 16) {
-        if (c0 >= NP) continue;
-        uint32_t v[16];
+      for (int mt = 0; mt < MT; ++mt) {
         if (ntiles > 0) {
-          tmem_ld16(tq + S::COL_O + mt * NMAX + c0, v);
-          tmem_wait_ld();
+          tmem_ld8(tq + S::COL_O + mt * NMAX + rbase + c, v[mt]);
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = 0u;
+          for (int j = 0; j < 8; ++j) v[mt][j] = 0u;
         }
+      }
+      if (ntiles > 0) tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int r = c0 + j;
-          if (r >= R) continue;
-          const float L = lsum[r] + lsum[NMAX + r] + lsum[2 * NMAX + r] + lsum[3 * NMAX + r];
-          const float M = m_ref[r];
-          const bool has = alive && ntiles > 0 && (M != -CUDART_INF_F) && (L > 0.f);
-          const float o = has ? __uint_as_float(v[j]) * vscale / L : 0.f;
-          const int t = r / p.G, jj = r - t * p.G;
-          const size_t grow = (static_cast<size_t>(b) * p.T + t) * p.num_q_heads + kvh * p.G + jj;
-          const float lse_val = has ? (M + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
+      for (int j = 0; j < 8; ++j) {
+        const int r = rbase + c + j;
+        if (r >= R) break;
+        const float sc = rscale[r];
+        const size_t grow = static_cast<size_t>(out_row[r]);
+        if constexpr (MT == 2) {
+          const float o0 = sc != 0.f ? __uint_as_float(v[0][j]) * sc : 0.f;
+          const float o1 = sc != 0.f ? __uint_as_float(v[1][j]) * sc : 0.f;
+          const int d0 = 2 * key_lane;
           if (final_out) {
-            p.out[grow * D + d_out] = __float2half_rn(o);
-            if (d_out == 0) p.lse[grow] = lse_val;
+            *reinterpret_cast<__half2*>(p.out + grow * D + d0) = __floats2half2_rn(o0, o1);
           } else {
-            p.o_part[(grow * p.num_splits + split) * D + d_out] = o;
-            if (d_out == 0) p.lse_part[grow * p.num_splits + split] = lse_val;
+            *reinterpret_cast<float2*>(p.o_part + (grow * p.num_splits + split) * D + d0) = make_float2(o0, o1);
+          }
+        } else {
+          const float o0 = sc != 0.f ? __uint_as_float(v[0][j]) * sc : 0.f;
+          if (final_out) {
+            p.out[grow * D + key_lane] = __float2half_rn(o0);
+          } else {
+            p.o_part[(grow * p.num_splits + split) * D + key_lane] = o0;
           }
         }
       }
     }
+    // last TMEM access of this warp done: the MMA warp may free TMEM
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tmem_done);
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   }
-  // all roles done with TMEM before it is released
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(S::TMEM_COLS));
+  if (warp == 1) {
+    // Free TMEM once the softmax warps (the last readers; the MMAs they waited for and the V
+    // converters' stores precede their reads) are done. Every softmax path arrives once, and
+    // their own waits are bounded, so this wait ends; a few limits' worth covers them.
+    bool got = false;
+    for (int k = 0; k < 4 && !got; ++k) got = mbar_wait(tmem_done, 0);
+    if (!got && lane == 0) atomicOr(p.err, kDevErrTimeout);
+    tc_fence_after();
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(S::TMEM_COLS));
+  }
 }
 
 }  // namespace pfkv
