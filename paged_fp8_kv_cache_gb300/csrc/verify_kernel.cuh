@@ -9,23 +9,29 @@
 //               two shared-memory rings (same tensor maps as the decode kernel);
 //   warp 1      MMA issuer (one lane) and TMEM owner;
 //   warps 2-9   softmax: each thread owns one key of the tile (its TMEM lane)
-//               and half of the query rows; it reads the key's logits from
-//               TMEM, masks, exponentiates against a per-row reference maximum
-//               and writes P^T (fp16) into a swizzled shared-memory B operand;
-//               at the end it reads O^T back from TMEM and writes the output;
+//               and half of the query rows; it pulls the key's logits from
+//               TMEM into registers (releasing the single S^T buffer to the
+//               next tile's MMAs), masks, exponentiates against a per-row
+//               reference maximum and writes P^T (fp16) into a swizzled
+//               shared-memory B operand; at the end it reads O^T back from
+//               TMEM and writes the output;
 //   warps 10-13 V converter: each thread owns one TMEM lane = one or two
 //               head-dim elements and writes them for all keys of the tile,
 //               FP8 -> fp16 (exact), as the A operand of O^T = V^T P^T
-//               (two TMEM buffers, so tile i+1 is converted while the MMAs of
-//               tile i run).
+//               (two TMEM buffers where they fit, so tile i+1 is converted
+//               while the MMAs of tile i run).
 // S^T = K Q^T runs on FP8 directly (tcgen05.mma kind::f8f6f4, M = 128 keys):
 // the K tile is the A operand exactly as TMA left it in shared memory, and Q
 // is the sum of three E4M3 terms per element (row r scaled by 2^e_r so that
 // its largest element is at most 448; the terms are the successive
 // round-to-nearest residuals, so their sum is the fp16 Q element to within
-// half an E4M3 subnormal step). The three term MMAs accumulate into one f32
-// accumulator. O^T = V^T P^T runs on kind::f16 (M = 128 head-dim elements).
-// N = query rows padded to 32/48/64.
+// half an E4M3 subnormal step). The terms are stacked along N (one MMA of
+// N = 3 x rows per 32 head-dim elements reads the K tile once); the softmax
+// adds the three columns. O^T = V^T P^T runs on kind::f16 (M = 128 head-dim
+// elements, N = rows). Rows are padded to 32/48/64.
+// The tensor pipe costs about the same per MMA instruction for any N up to
+// ~144 at these shapes, so the instruction count, not the FLOPs, is what
+// the MMA schedule minimises.
 // Online softmax: every row keeps a reference maximum m; p is formed against
 // it in one pass. A tile whose logits exceed m by more than kRescaleLog2
 // triggers an exact update (the tile's row maxima are reduced across the 128
@@ -49,6 +55,9 @@
 namespace pfkv {
 
 constexpr float kRescaleLog2 = 8.f;
+// Reference maximum of a row that has seen no visible key yet: finite, so that logit minus
+// reference is +1e30 for a visible key (forcing an update) and -inf for a masked one (p = 0).
+constexpr float kNoRef = -1e30f;
 constexpr int kQTerms = 3;
 constexpr int kSoftmaxWarps = 8;
 
@@ -60,16 +69,19 @@ struct VerifyShape {
   static constexpr int KV_TILE = NBOX * SUB;             // K (or V) bytes per tile
   static constexpr int NMAX = NMAX_;                     // padded query rows (MMA N): 32, 48 or 64
   static constexpr int HN = NMAX / 2;                    // rows per softmax warp
-  static constexpr int QT_BYTES = NBOX * NMAX * 128;     // one E4M3 term of Q: D/128 blocks of NMAX x 128 B
-  static constexpr int Q_BYTES = kQTerms * QT_BYTES;
+  static constexpr int NQ = kQTerms * NMAX;               // B rows of S^T: term t of row r is row t*NMAX + r
+  static constexpr int Q_BLK = NQ * 128;                 // one 128-dim block of the stacked Q terms
+  static constexpr int Q_BYTES = NBOX * Q_BLK;
   static constexpr int PT_BYTES = (KT / 64) * NMAX * 128;  // one P^T buffer (fp16, K-major, 64-key blocks)
   static constexpr int MT = D / 128;                     // O^T M-tiles
   static constexpr int TMEM_COLS = 512;
-  static constexpr int COL_S = 0;                        // 2 x NMAX: S^T double buffer
-  static constexpr int COL_O = 2 * NMAX;                 // MT x NMAX: O^T
-  static constexpr int COL_AV = ((COL_O + MT * NMAX + 31) / 32) * 32;  // 2 x AV_COLS: V^T operands
+  static constexpr int COL_S = 0;                        // NQ: S^T, one column group per Q term
+  static constexpr int COL_O = NQ;                       // MT x NMAX: O^T
+  static constexpr int COL_AV = ((COL_O + MT * NMAX + 31) / 32) * 32;  // NAV x AV_COLS: V^T operands
   static constexpr int AV_COLS = MT * KT / 2;            // one V^T operand (fp16 pairs)
-  static_assert(COL_AV + 2 * AV_COLS <= TMEM_COLS, "TMEM budget");
+  static constexpr int NAV = COL_AV + 2 * AV_COLS <= TMEM_COLS ? 2 : 1;
+  static_assert(COL_AV + NAV * AV_COLS <= TMEM_COLS, "TMEM budget");
+  static_assert(NQ <= 256, "MMA N");
   static_assert(HN % 8 == 0, "softmax rows come in TMEM loads of 8 columns");
   // misc: m_ref, alpha, sc2r, rscale, wred[4], lsum[4] (NMAX floats each), out_row (NMAX ints),
   // vote flags, TMEM slot, barriers
@@ -213,7 +225,6 @@ __global__ void __launch_bounds__(448, 1)
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int R = p.T * p.G;
-  const int NP = (R + 15) & ~15;  // MMA N
 
   // launched with programmatic stream serialisation: wait for the preceding grid first
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -245,11 +256,11 @@ __global__ void __launch_bounds__(448, 1)
   uint64_t* kempty = kfull + NK;       // [NK] MMA commit: S^T MMAs done reading the K tile
   uint64_t* vfull = kempty + NK;       // [NV] producer -> V converter
   uint64_t* vempty = vfull + NV;       // [NV] V converter -> producer
-  uint64_t* av_full = vempty + NV;     // [2] V converter -> MMA (V^T operand written)
-  uint64_t* av_free = av_full + 2;     // [2] MMA commit: O^T MMAs done with a V^T operand
-  uint64_t* s_full = av_free + 2;      // [2] MMA commit: S^T ready
-  uint64_t* s_free = s_full + 2;       // [2] softmax -> MMA: S^T read
-  uint64_t* pt_full = s_free + 2;      // [2] softmax -> MMA: P^T written
+  uint64_t* av_full = vempty + NV;     // [NAV] V converter -> MMA (V^T operand written)
+  uint64_t* av_free = av_full + 2;     // [NAV] MMA commit: O^T MMAs done with a V^T operand
+  uint64_t* s_full = av_free + 2;      // MMA commit: S^T ready
+  uint64_t* s_free = s_full + 1;       // softmax -> MMA: S^T read into registers
+  uint64_t* pt_full = s_free + 1;      // [2] softmax -> MMA: P^T written
   uint64_t* pt_free = pt_full + 2;     // [2] MMA commit: O^T MMAs of the tile done (P^T buffer free)
   uint64_t* swg_bar = pt_free + 2;     // softmax warps' rendezvous (bounded waits, unlike bar.sync)
   uint64_t* tmem_done = swg_bar + 1;   // softmax warps -> MMA warp: last TMEM read done
@@ -269,11 +280,11 @@ __global__ void __launch_bounds__(448, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&av_full[i], 4);
       mbar_init(&av_free[i], 1);
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], kSoftmaxWarps);
       mbar_init(&pt_full[i], kSoftmaxWarps);
       mbar_init(&pt_free[i], 1);
     }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, kSoftmaxWarps);
     mbar_init(swg_bar, kSoftmaxWarps);
     mbar_init(tmem_done, kSoftmaxWarps);
     fence_barrier_init();
@@ -288,7 +299,7 @@ __global__ void __launch_bounds__(448, 1)
   // Q -> three E4M3 terms in shared memory (K-major, 128B swizzle), one warp per row; padded rows zero
   {
     constexpr int PER_LANE = D / 32;  // 8 (D = 256) or 4 (D = 128) consecutive dims per lane
-    for (int r = warp; r < NP; r += 14) {
+    for (int r = warp; r < NMAX; r += 14) {
       float x[PER_LANE];
       float mx = 0.f;
       if (r < R) {
@@ -335,10 +346,11 @@ __global__ void __launch_bounds__(448, 1)
         for (int k = 0; k < kQTerms; ++k) tw[k][i / 4] = (lo[k] & 0xFFFFu) | (hi[k] << 16);
       }
       const int d0 = lane * PER_LANE;
-      const int off = (d0 >> 7) * NMAX * 128 + r * 128 + (((((d0 & 127) >> 4) ^ r) & 7) << 4) + (d0 & 15);
+      // term k of row r is B row k * NMAX + r (NMAX is a multiple of 8: same swizzle phase)
+      const int off = (d0 >> 7) * S::Q_BLK + r * 128 + (((((d0 & 127) >> 4) ^ r) & 7) << 4) + (d0 & 15);
 #pragma unroll
       for (int k = 0; k < kQTerms; ++k) {
-        unsigned char* dst = smem + S::OFF_Q + k * S::QT_BYTES + off;
+        unsigned char* dst = smem + S::OFF_Q + k * NMAX * 128 + off;
         if constexpr (PER_LANE == 8) {
           *reinterpret_cast<uint2*>(dst) = make_uint2(tw[k][0], tw[k][1]);
         } else {
@@ -346,7 +358,7 @@ __global__ void __launch_bounds__(448, 1)
         }
       }
     }
-    for (int i = tid; i < NMAX; i += blockDim.x) m_ref[i] = -CUDART_INF_F;
+    for (int i = tid; i < NMAX; i += blockDim.x) m_ref[i] = kNoRef;
     if (tid == 0) flag[0] = flag[1] = flag[2] = 0;
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -460,13 +472,16 @@ __global__ void __launch_bounds__(448, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && ntiles > 0) {
-      const uint32_t idesc_qk = umma_idesc_f8(NP, KV == kKvE4m3 ? 0u : 1u);
-      const uint32_t idesc_pv = umma_idesc_f16(NP);
-      const uint32_t q_base = smem_u32(smem + S::OFF_Q);
-      const uint32_t k_base = smem_u32(smem + S::OFF_KRING);
-      const uint32_t pt_base = smem_u32(smem + S::OFF_PT);
-      // Issue whichever MMA group is ready: S^T of the next tile (its K tile landed, its S
-      // buffer released by the softmax) or O^T of the oldest tile whose V^T operand and P^T
+      constexpr int NAV = S::NAV;
+      const uint32_t idesc_qk = umma_idesc_f8(S::NQ, KV == kKvE4m3 ? 0u : 1u);
+      const uint32_t idesc_pv = umma_idesc_f16(NMAX);
+      // descriptors of the operands' first k-slices; a k-step adds its byte offset / 16 to the
+      // start-address field (every operand lies below 256 KB, so the 14-bit field never carries)
+      const uint64_t q_desc = umma_desc_sw128(smem_u32(smem + S::OFF_Q));
+      const uint64_t k_desc = umma_desc_sw128(smem_u32(smem + S::OFF_KRING));
+      const uint64_t pt_desc = umma_desc_sw128(smem_u32(smem + S::OFF_PT));
+      // Issue whichever MMA group is ready: S^T of the next tile (its K tile landed, the S^T
+      // buffer read out by the softmax) or O^T of the oldest tile whose V^T operand and P^T
       // are written. Neither waits behind the other.
       int sn = 0, on = 0;
       bool ok = true;
@@ -474,39 +489,34 @@ __global__ void __launch_bounds__(448, 1)
       while (on < ntiles) {
         bool progress = false;
         if (sn < ntiles && mbar_test(&kfull[sn % NK], (sn / NK) & 1) &&
-            (sn < 2 || mbar_test(&s_free[sn & 1], ((sn >> 1) - 1) & 1))) {
+            (sn == 0 || mbar_test(s_free, (sn - 1) & 1))) {
           tc_fence_after();
-          const uint32_t d_t = tbase + S::COL_S + (sn & 1) * NMAX;
-          const uint32_t ka = k_base + (sn % NK) * S::KV_TILE;
-#pragma unroll 1
-          for (int ks = 0; ks < D / 32; ++ks) {  // 32 FP8 dims = 32 bytes of a swizzled row per MMA
-            const uint64_t ad = umma_desc_sw128(ka + (ks >> 2) * S::SUB + (ks & 3) * 32);
+          const uint64_t ka = k_desc + static_cast<uint64_t>(((sn % NK) * S::KV_TILE) >> 4);
 #pragma unroll
-            for (int k = 0; k < kQTerms; ++k) {
-              const uint64_t bd = umma_desc_sw128(q_base + k * S::QT_BYTES + (ks >> 2) * NMAX * 128 + (ks & 3) * 32);
-              umma_ss_f8(d_t, ad, bd, idesc_qk, (ks > 0 || k > 0) ? 1u : 0u);
-            }
+          for (int ks = 0; ks < D / 32; ++ks) {  // 32 FP8 dims = 32 bytes of a swizzled row per MMA
+            const uint32_t koff = ((ks >> 2) * S::SUB + (ks & 3) * 32) >> 4;
+            const uint32_t qoff = ((ks >> 2) * S::Q_BLK + (ks & 3) * 32) >> 4;
+            umma_ss_f8(tbase + S::COL_S, ka + koff, q_desc + qoff, idesc_qk, ks > 0 ? 1u : 0u);
           }
-          umma_commit(&s_full[sn & 1]);
+          umma_commit(s_full);
           umma_commit(&kempty[sn % NK]);
           ++sn;
           progress = true;
         }
-        if (on < sn && mbar_test(&av_full[on & 1], (on >> 1) & 1) && mbar_test(&pt_full[on & 1], (on >> 1) & 1)) {
+        if (on < sn && mbar_test(&av_full[on % NAV], (on / NAV) & 1) && mbar_test(&pt_full[on & 1], (on >> 1) & 1)) {
           tc_fence_after();
-          const uint32_t pt = pt_base + (on & 1) * S::PT_BYTES;
-          const uint32_t av = tbase + S::COL_AV + (on & 1) * S::AV_COLS;
+          const uint64_t pt = pt_desc + static_cast<uint64_t>(((on & 1) * S::PT_BYTES) >> 4);
+          const uint32_t av = tbase + S::COL_AV + (on % NAV) * S::AV_COLS;
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll 1
-            for (int ks = 0; ks < KT / 16; ++ks) {
-              const uint64_t bd = umma_desc_sw128(pt + (ks >> 2) * NMAX * 128 + (ks & 3) * 32);
-              umma_ts(tbase + S::COL_O + mt * NMAX, av + mt * (KT / 2) + 8 * ks, bd, idesc_pv,
+          for (int ks = 0; ks < KT / 16; ++ks) {
+            const uint32_t poff = ((ks >> 2) * NMAX * 128 + (ks & 3) * 32) >> 4;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+              umma_ts(tbase + S::COL_O + mt * NMAX, av + mt * (KT / 2) + 8 * ks, pt + poff, idesc_pv,
                       (on > 0 || ks > 0) ? 1u : 0u);
-            }
           }
           umma_commit(&pt_free[on & 1]);
-          umma_commit(&av_free[on & 1]);
+          umma_commit(&av_free[on % NAV]);
           ++on;
           progress = true;
         }
@@ -538,15 +548,16 @@ __global__ void __launch_bounds__(448, 1)
     for (int j = 0; j < 8; ++j) voff[j] = vbx * S::SUB + swz_offset(j, vbyte >> 4) + (vbyte & 15);
     for (int it = 0; it < ntiles; ++it) {
       const int s = it % NV;
-      // V^T buffer it&1 is free once the O^T MMAs of tile it-2 are done (sound: this thread
-      // saw that barrier's previous phase, of tile it-4, before converting tile it-2)
-      if (!mbar_wait(&vfull[s], (it / NV) & 1) || (it >= 2 && !mbar_wait(&av_free[it & 1], ((it >> 1) - 1) & 1))) {
+      // V^T buffer it % NAV is free once the O^T MMAs of tile it-NAV are done (sound: this thread
+      // saw that barrier's previous phase, of tile it-2*NAV, before converting tile it-NAV)
+      if (!mbar_wait(&vfull[s], (it / NV) & 1) ||
+          (it >= S::NAV && !mbar_wait(&av_free[it % S::NAV], ((it / S::NAV) - 1) & 1))) {
         alive = false;
         break;
       }
       tc_fence_after();
       const unsigned char* Vs = smem + S::OFF_VRING + s * S::KV_TILE;
-      const uint32_t av = tq + S::COL_AV + (it & 1) * S::AV_COLS;
+      const uint32_t av = tq + S::COL_AV + (it % S::NAV) * S::AV_COLS;
       const int valid = min(KT, t1 - (t0 + it * KT));
       const bool tail = valid < KT;
 #pragma unroll 1
@@ -580,7 +591,7 @@ __global__ void __launch_bounds__(448, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&av_full[it & 1]);
+        mbar_arrive(&av_full[it % S::NAV]);
         mbar_arrive(&vempty[s]);
       }
     }
@@ -617,44 +628,54 @@ __global__ void __launch_bounds__(448, 1)
       m[6] = c.z;
       m[7] = c.w;
     };
-    // 2^(s - m) against a reference m; 0 while a row has no reference yet, and capped so
-    // that a logit that outgrew its reference (the tile is then redone) stays finite
-    auto pexp = [](float s2, float m) -> float {
-      return m == -CUDART_INF_F ? 0.f : fast_exp2(fminf(s2 - m, 15.f));
-    };
+    // 2^(s - m) for x = s - m (base-2 units), capped so that a logit that outgrew its reference
+    // stays finite (the tile is then redone). A row without a reference yet has m = kNoRef, so x
+    // is 1e30 for a visible key, p = 2^15 and x > kRescaleLog2: such a tile always takes the
+    // update, whose factor for that row is 2^(kNoRef - m) = 0, and is redone.
+    auto pexp = [](float x) -> float { return fast_exp2(fminf(x, 15.f)); };
     for (int it = 0; it < ntiles && alive; ++it) {
       const int sb = it & 1;
-      if (!mbar_wait(&s_full[sb], (it >> 1) & 1)) {
+      if (!mbar_wait(s_full, it & 1)) {
         alive = false;
         break;
       }
       tc_fence_after();
-      // P^T buffer sb is free once the O^T MMAs of tile it-2 are done
-      if (it >= 2 && !mbar_wait(&pt_free[sb], ((it >> 1) - 1) & 1)) {
-        alive = false;
-        break;
-      }
-      const uint32_t s_col = tq + S::COL_S + sb * NMAX + rbase;
       const int tile_start = t0 + it * KT;
       const int kp = tile_start + key_lane;  // absolute key position
       const bool in_range = kp < t1;
       // row r sees this key iff r / G >= kp - (N - T), i.e. r >= G * (kp - (N - T))
       const int rmin = p.G * (kp - tlim_base);
       const bool all_vis = (tile_start + KT <= t1) && (tile_start + KT - 1 <= tlim_base);  // CTA-uniform
-      // logits of rows rbase+c .. rbase+c+7 of this thread's key, in base-2 units, masked
-      auto load_s2 = [&](int c, float (&s2)[8]) {
-        uint32_t v[8];
+      // this key's logits of rows rbase .. rbase+HN-1 (sum of the three Q-term columns), in
+      // base-2 units, -inf where masked; then the S^T buffer goes back to the MMA warp
+      float s2[HN];
+#pragma unroll
+      for (int c = 0; c < HN; c += 8) {
+        uint32_t v0[8], v1[8], v2[8];
         float sc[8];
-        tmem_ld8(s_col + c, v);
+        const uint32_t col = tq + S::COL_S + rbase + c;
+        tmem_ld8(col, v0);
+        tmem_ld8(col + NMAX, v1);
+        tmem_ld8(col + 2 * NMAX, v2);
         load8(sc2r + rbase + c, sc);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int r = rbase + c + j;
           const bool vis = all_vis || (in_range && (r >= R || r >= rmin));
-          s2[j] = vis ? __uint_as_float(v[j]) * sc[j] : -CUDART_INF_F;
+          const float raw = (__uint_as_float(v0[j]) + __uint_as_float(v1[j])) + __uint_as_float(v2[j]);
+          s2[c + j] = vis ? raw * sc[j] : -CUDART_INF_F;
         }
-      };
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
+      // P^T buffer sb is free once the O^T MMAs of tile it-2 are done (sound: this thread saw
+      // that barrier's previous phase, of tile it-4, at tile it-2)
+      if (it >= 2 && !mbar_wait(&pt_free[sb], ((it >> 1) - 1) & 1)) {
+        alive = false;
+        break;
+      }
       unsigned char* pt = smem + S::OFF_PT + sb * S::PT_BYTES + (key_lane >> 6) * NMAX * 128;
       const int kk = key_lane & 63;
       bool update = (it == 0);  // the first tile has no references yet
@@ -666,26 +687,25 @@ __global__ void __launch_bounds__(448, 1)
           // terms (same formula, same values) taken back out of the row sums
 #pragma unroll
           for (int c = 0; c < HN; c += 8) {
-            float s2[8], m[8];
-            load_s2(c, s2);
+            float m[8];
             load8(m_ref + rbase + c, m);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              float mx = s2[j];
+              float mx = s2[c + j];
 #pragma unroll
               for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
               if (lane == 0) wred[q * NMAX + rbase + c + j] = mx;
-              if (did_pass) l_part[c + j] -= pexp(s2[j], m[j]);
+              if (did_pass) l_part[c + j] -= pexp(s2[c + j] - m[j]);
             }
           }
           swg_sync();
-          if (sidx < NP) {
+          if (sidx < NMAX) {
             const int r = sidx;
             const float mt = fmaxf(fmaxf(wred[r], wred[NMAX + r]), fmaxf(wred[2 * NMAX + r], wred[3 * NMAX + r]));
             const float mo = m_ref[r];
             const float mn = fmaxf(mo, mt);
-            // the reference only moves up; rows with nothing visible so far keep -inf
-            alpha_s[r] = (mo == -CUDART_INF_F) ? 0.f : fast_exp2(mo - mn);
+            // the reference only moves up; rows with nothing visible so far keep kNoRef
+            alpha_s[r] = fast_exp2(mo - mn);
             m_ref[r] = mn;
           }
           swg_sync();
@@ -723,13 +743,13 @@ __global__ void __launch_bounds__(448, 1)
         bool exceed = false;
 #pragma unroll
         for (int c = 0; c < HN; c += 8) {
-          float s2[8], m[8];
-          load_s2(c, s2);
+          float m[8];
           load8(m_ref + rbase + c, m);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            exceed |= (s2[j] > m[j] + kRescaleLog2);
-            const float pr = pexp(s2[j], m[j]);
+            const float x = s2[c + j] - m[j];
+            exceed |= (x > kRescaleLog2);
+            const float pr = pexp(x);
             l_part[c + j] += pr;
             *reinterpret_cast<__half*>(pt + sw128_elem(rbase + c + j, kk)) = __float2half_rn(pr);
           }
@@ -745,9 +765,8 @@ __global__ void __launch_bounds__(448, 1)
         if (sidx == 0) flag[(it + 2) % 3] = 0;
         if (!update) break;
       }
+      if (!alive) break;
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);  // S^T buffer sb fully read
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(&pt_full[sb]);
@@ -773,7 +792,7 @@ __global__ void __launch_bounds__(448, 1)
       const int r = sidx;
       const float L = lsum[r] + lsum[NMAX + r] + lsum[2 * NMAX + r] + lsum[3 * NMAX + r];
       const float M = m_ref[r];
-      const bool has = alive && ntiles > 0 && (M != -CUDART_INF_F) && (L > 0.f);
+      const bool has = alive && ntiles > 0 && (M != kNoRef) && (L > 0.f);
       const int t = r / p.G, jj = r - t * p.G;
       const int grow = (b * p.T + t) * p.num_q_heads + kvh * p.G + jj;
       rscale[r] = has ? vscale / L : 0.f;
