@@ -9,7 +9,9 @@ any), the split-KV decode kernel and the LSE merge, all through the C ABI
 
 Prints ONE JSON line (rank 0). ``value`` = algorithmic bytes of all ranks /
 max-over-ranks device time of the K timed steps (inputs resident in HBM, L2
-flushed between steps). ``e2e`` repeats the measurement through the same
+flushed between steps: a 256 MiB write, then a 256 MiB read, so that the
+step starts on a cold L2 holding no dirty lines, whose write-back would
+otherwise compete with the step's own HBM traffic). ``e2e`` repeats the measurement through the same
 public calls with the step's inputs copied from pinned host memory and the
 outputs copied back inside the timed region. ``--impl reference`` times the
 CPU oracle (the only reference arm this project has) on a bounded sample.
@@ -49,6 +51,22 @@ KERNEL_SOURCES = ["decode_kernel.cuh", "device_utils.cuh", "frag_layout.h"]  # t
 
 
 # ----------------------------------------------------------------------------- helpers
+
+
+class L2Flush:
+    """Cold, clean L2 before a timed step: write a buffer larger than L2, then read another
+    (the write-back of the written lines happens during the read, outside the timed region)."""
+
+    def __init__(self, torch):
+        n = L2_FLUSH_BYTES // 4
+        self.torch = torch
+        self.w = torch.zeros(n, dtype=torch.float32, device="cuda")
+        self.r = torch.ones(n, dtype=torch.float32, device="cuda")
+        self.sink = torch.zeros((), dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        self.w.add_(1)
+        self.torch.sum(self.r, dim=0, out=self.sink)
 
 def algorithmic_bytes(case, with_append: bool) -> int:
     s = case.spec
@@ -256,14 +274,14 @@ def time_steps(dw, torch, K, W, flush, e2e=False):
             dw.d2h()
 
     for _ in range(W):
-        flush.add_(1)
+        flush()
         step()
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     for i in range(K):
-        flush.add_(1)
+        flush()
         starts[i].record()
         step(mids[i])
         ends[i].record()
@@ -298,7 +316,7 @@ def run_gpu(args):
     spec = workloads.CONFIGS[wid]
     case = workloads.make_case(spec, seed=rank_seed(spec, rank))
     dw = DeviceWorkload(case, torch, pf)
-    flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    flush = L2Flush(torch)
     nbytes = algorithmic_bytes(case, dw.has_append)
     pf.pfkv_device_errors(clear=True)
 
@@ -343,7 +361,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "f16 mma / f32 accumulate over " + {"fp16": "fp16", "e4m3": "fp8-e4m3", "e5m2": "fp8-e5m2"}[spec.kv_dtype] + " KV",
         "data": "synthetic (seeded generator, " + spec.name + ")",
-        "config": {"workload": spec.name, "workload_id": wid, "l2": "flushed before every step (256 MiB write)",
+        "config": {"workload": spec.name, "workload_id": wid, "l2": "flushed before every step (256 MiB write, then 256 MiB read: cold and clean)",
                    "algorithmic_bytes_per_step": nbytes, "num_splits": dw.splits, "split_tokens": dw.split_tokens,
                    "parallelism": f"replicas x{world} (independent batches, no collective on the data path)"},
         "calls_per_s": round(args.steps / (total_ms * 1e-3), 1),

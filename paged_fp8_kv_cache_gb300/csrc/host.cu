@@ -240,8 +240,10 @@ pfkv_status make_plan(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_k
     const int target = sms * ctas_per_sm(dev, pl->cfg, pl->ncw, pl->tc, pl->nmax);
     const int base = (target + units - 1) / units;
     // bound the keys per CTA so ragged batches balance; the bound grows with
-    // the row count because every range costs an fp32 partial per row
-    const int max_keys = R * 256 > 2048 ? R * 256 : 2048;
+    // the row count because every range costs an fp32 partial per row, and doubles
+    // for the tcgen05 kernel (one CTA per SM, with a fixed start-up and first-tile cost
+    // worth ~8 tiles: two waves of half-length ranges cost more than one wave)
+    const int max_keys = (pl->tc ? 2 : 1) * (R * 256 > 2048 ? R * 256 : 2048);
     const int need = (max_seq_len + max_keys - 1) / max_keys;
     const int k = base > 0 ? (need + base - 1) / base : 1;
     want = base * (k > 1 ? k : 1);

@@ -60,6 +60,7 @@ constexpr float kRescaleLog2 = 8.f;
 constexpr float kNoRef = -1e30f;
 constexpr int kQTerms = 3;
 constexpr int kSoftmaxWarps = 8;
+constexpr int kVerifyWarps = 14;
 
 template <int D, int NMAX_>
 struct VerifyShape {
@@ -214,8 +215,9 @@ __device__ __forceinline__ void split3_e4m3(float x0, float x1, uint32_t (&t)[kQ
   }
 }
 
+// 14 warps: the busiest SM sub-partition holds 4 of them, which caps a thread at 128 registers
 template <int D, int KV, int NMAX_>
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(kVerifyWarps * 32, 1)
     verify_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeParams p) {
   using S = VerifyShape<D, NMAX_>;
@@ -299,7 +301,7 @@ __global__ void __launch_bounds__(448, 1)
   // Q -> three E4M3 terms in shared memory (K-major, 128B swizzle), one warp per row; padded rows zero
   {
     constexpr int PER_LANE = D / 32;  // 8 (D = 256) or 4 (D = 128) consecutive dims per lane
-    for (int r = warp; r < NMAX; r += 14) {
+    for (int r = warp; r < NMAX; r += kVerifyWarps) {
       float x[PER_LANE];
       float mx = 0.f;
       if (r < R) {
@@ -480,55 +482,53 @@ __global__ void __launch_bounds__(448, 1)
       const uint64_t q_desc = umma_desc_sw128(smem_u32(smem + S::OFF_Q));
       const uint64_t k_desc = umma_desc_sw128(smem_u32(smem + S::OFF_KRING));
       const uint64_t pt_desc = umma_desc_sw128(smem_u32(smem + S::OFF_PT));
-      // Issue whichever MMA group is ready: S^T of the next tile (its K tile landed, the S^T
-      // buffer read out by the softmax) or O^T of the oldest tile whose V^T operand and P^T
-      // are written. Neither waits behind the other.
-      int sn = 0, on = 0;
+      // With one S^T buffer the order is fixed: S^T(0), then per tile i: S^T(i+1) (its K tile
+      // landed, S^T(i) read out by the softmax, which happens at the start of tile i), then
+      // O^T(i) (V^T(i) and P^T(i) written, at the end of tile i). Blocking waits wake as soon as
+      // the phase completes. Each parity wait is sound: this thread saw the previous phase of
+      // that barrier, and its next phase needs an MMA this thread has not issued yet.
+      // (Issuing the O^T MMAs from a second warp was measured slower: that warp's sub-partition
+      // also runs a V converter, which then fell behind.)
       bool ok = true;
-      uint64_t last = global_ns();
-      while (on < ntiles) {
-        bool progress = false;
-        if (sn < ntiles && mbar_test(&kfull[sn % NK], (sn / NK) & 1) &&
-            (sn == 0 || mbar_test(s_free, (sn - 1) & 1))) {
+      auto issue_s = [&](int sn) {
+        const uint64_t ka = k_desc + static_cast<uint64_t>(((sn % NK) * S::KV_TILE) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < D / 32; ++ks) {  // 32 FP8 dims = 32 bytes of a swizzled row per MMA
+          const uint32_t koff = ((ks >> 2) * S::SUB + (ks & 3) * 32) >> 4;
+          const uint32_t qoff = ((ks >> 2) * S::Q_BLK + (ks & 3) * 32) >> 4;
+          umma_ss_f8(tbase + S::COL_S, ka + koff, q_desc + qoff, idesc_qk, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(s_full);
+        umma_commit(&kempty[sn % NK]);
+      };
+      ok = mbar_wait(&kfull[0], 0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int on = 0; on < ntiles && ok; ++on) {
+        const int sn = on + 1;
+        if (sn < ntiles) {
+          ok = mbar_wait(&kfull[sn % NK], (sn / NK) & 1) && mbar_wait(s_free, (sn - 1) & 1);
+          if (!ok) break;
           tc_fence_after();
-          const uint64_t ka = k_desc + static_cast<uint64_t>(((sn % NK) * S::KV_TILE) >> 4);
-#pragma unroll
-          for (int ks = 0; ks < D / 32; ++ks) {  // 32 FP8 dims = 32 bytes of a swizzled row per MMA
-            const uint32_t koff = ((ks >> 2) * S::SUB + (ks & 3) * 32) >> 4;
-            const uint32_t qoff = ((ks >> 2) * S::Q_BLK + (ks & 3) * 32) >> 4;
-            umma_ss_f8(tbase + S::COL_S, ka + koff, q_desc + qoff, idesc_qk, ks > 0 ? 1u : 0u);
-          }
-          umma_commit(s_full);
-          umma_commit(&kempty[sn % NK]);
-          ++sn;
-          progress = true;
+          issue_s(sn);
         }
-        if (on < sn && mbar_test(&av_full[on % NAV], (on / NAV) & 1) && mbar_test(&pt_full[on & 1], (on >> 1) & 1)) {
-          tc_fence_after();
-          const uint64_t pt = pt_desc + static_cast<uint64_t>(((on & 1) * S::PT_BYTES) >> 4);
-          const uint32_t av = tbase + S::COL_AV + (on % NAV) * S::AV_COLS;
+        ok = mbar_wait(&av_full[on % NAV], (on / NAV) & 1) && mbar_wait(&pt_full[on & 1], (on >> 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t pt = pt_desc + static_cast<uint64_t>(((on & 1) * S::PT_BYTES) >> 4);
+        const uint32_t av = tbase + S::COL_AV + (on % NAV) * S::AV_COLS;
 #pragma unroll
-          for (int ks = 0; ks < KT / 16; ++ks) {
-            const uint32_t poff = ((ks >> 2) * NMAX * 128 + (ks & 3) * 32) >> 4;
+        for (int ks = 0; ks < KT / 16; ++ks) {
+          const uint32_t poff = ((ks >> 2) * NMAX * 128 + (ks & 3) * 32) >> 4;
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-              umma_ts(tbase + S::COL_O + mt * NMAX, av + mt * (KT / 2) + 8 * ks, pt + poff, idesc_pv,
-                      (on > 0 || ks > 0) ? 1u : 0u);
-          }
-          umma_commit(&pt_free[on & 1]);
-          umma_commit(&av_free[on % NAV]);
-          ++on;
-          progress = true;
+          for (int mt = 0; mt < MT; ++mt)
+            umma_ts(tbase + S::COL_O + mt * NMAX, av + mt * (KT / 2) + 8 * ks, pt + poff, idesc_pv,
+                    (on > 0 || ks > 0) ? 1u : 0u);
         }
-        if (progress) {
-          last = global_ns();
-        } else {
-          if (global_ns() - last > kWaitLimitNs) {
-            ok = false;
-            break;
-          }
-          __nanosleep(32);
-        }
+        umma_commit(&pt_free[on & 1]);
+        umma_commit(&av_free[on % NAV]);
       }
       if (!ok) atomicOr(p.err, kDevErrTimeout);
     }
@@ -580,9 +580,16 @@ __global__ void __launch_bounds__(448, 1)
             if (k0 + kk >= valid) wa = 0u;
             if (k0 + kk + 1 >= valid) wb = 0u;
           }
-          const uint32_t X = __byte_perm(wa, wb, 0x5140);  // [a.b0, b.b0, a.b1, b.b1]
-          v0[kk >> 1] = fp8x2_to_f16x2<KV>(X);
-          v1[kk >> 1] = fp8x2_to_f16x2<KV>(X >> 16);
+          if constexpr (KV == kKvE5m2 && D == 256) {
+            // an E5M2 code is the high byte of the fp16 with the same value: the fp16 pairs
+            // (key k, key k+1) of dims 2L and 2L+1 are byte moves, bytes 2-3 of wa being zero
+            v0[kk >> 1] = __byte_perm(wa, wb, 0x4202);  // [0, a.b0, 0, b.b0]
+            v1[kk >> 1] = __byte_perm(wa, wb, 0x5212);  // [0, a.b1, 0, b.b1]
+          } else {
+            const uint32_t X = __byte_perm(wa, wb, 0x5140);  // [a.b0, b.b0, a.b1, b.b1]
+            v0[kk >> 1] = fp8x2_to_f16x2<KV>(X);
+            v1[kk >> 1] = fp8x2_to_f16x2<KV>(X >> 16);
+          }
         }
         tmem_st16(av + (k0 >> 1), v0);
         if constexpr (MT == 2) tmem_st16(av + KT / 2 + (k0 >> 1), v1);
@@ -648,16 +655,19 @@ __global__ void __launch_bounds__(448, 1)
       const bool all_vis = (tile_start + KT <= t1) && (tile_start + KT - 1 <= tlim_base);  // CTA-uniform
       // this key's logits of rows rbase .. rbase+HN-1 (sum of the three Q-term columns), in
       // base-2 units, -inf where masked; then the S^T buffer goes back to the MMA warp
+      // and whether any of them exceeds its row's reference by more than kRescaleLog2
       float s2[HN];
+      bool exceed = false;
 #pragma unroll
       for (int c = 0; c < HN; c += 8) {
         uint32_t v0[8], v1[8], v2[8];
-        float sc[8];
+        float sc[8], m[8];
         const uint32_t col = tq + S::COL_S + rbase + c;
         tmem_ld8(col, v0);
         tmem_ld8(col + NMAX, v1);
         tmem_ld8(col + 2 * NMAX, v2);
         load8(sc2r + rbase + c, sc);
+        load8(m_ref + rbase + c, m);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -665,11 +675,22 @@ __global__ void __launch_bounds__(448, 1)
           const bool vis = all_vis || (in_range && (r >= R || r >= rmin));
           const float raw = (__uint_as_float(v0[j]) + __uint_as_float(v1[j])) + __uint_as_float(v2[j]);
           s2[c + j] = vis ? raw * sc[j] : -CUDART_INF_F;
+          exceed |= (s2[c + j] - m[j] > kRescaleLog2);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
+      // Vote on the update now and meet after the pass (which assumes no update): the
+      // rendezvous then costs nothing unless the warps are far apart. (Three rotating flags:
+      // the one cleared below, of tile it-1, was read by every thread before it voted on this
+      // tile, and is voted on again only after the next rendezvous, which the clearing thread
+      // must reach first.)
+      if (it > 0) {
+        if (__any_sync(0xffffffffu, exceed) && lane == 0) atomicOr(&flag[it % 3], 1);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(swg_bar);
+      }
       // P^T buffer sb is free once the O^T MMAs of tile it-2 are done (sound: this thread saw
       // that barrier's previous phase, of tile it-4, at tile it-2)
       if (it >= 2 && !mbar_wait(&pt_free[sb], ((it >> 1) - 1) & 1)) {
@@ -739,8 +760,7 @@ __global__ void __launch_bounds__(448, 1)
             tmem_wait_st();
           }
         }
-        // one pass: P^T and the row sums against the current references; note outgrown rows
-        bool exceed = false;
+        // one pass: P^T and the row sums against the current references
 #pragma unroll
         for (int c = 0; c < HN; c += 8) {
           float m[8];
@@ -748,7 +768,6 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float x = s2[c + j] - m[j];
-            exceed |= (x > kRescaleLog2);
             const float pr = pexp(x);
             l_part[c + j] += pr;
             *reinterpret_cast<__half*>(pt + sw128_elem(rbase + c + j, kk)) = __float2half_rn(pr);
@@ -756,11 +775,8 @@ __global__ void __launch_bounds__(448, 1)
         }
         did_pass = true;
         if (update) break;  // after an update no logit exceeds its reference
-        // (three rotating flags: the one cleared here, of tile it-1, was read by every
-        // thread before it reached this tile's rendezvous, and is voted on again only
-        // after the next rendezvous, which the clearing thread must reach first)
-        if (__any_sync(0xffffffffu, exceed) && lane == 0) atomicOr(&flag[it % 3], 1);
-        swg_sync();
+        if (!mbar_wait(swg_bar, swg_phase & 1)) alive = false;  // the vote cast before the pass
+        ++swg_phase;
         update = flag[it % 3] != 0;
         if (sidx == 0) flag[(it + 2) % 3] = 0;
         if (!update) break;

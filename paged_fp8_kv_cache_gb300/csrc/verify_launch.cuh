@@ -8,7 +8,7 @@
 
 namespace pfkv {
 
-constexpr int kVerifyThreads = 448;
+constexpr int kVerifyThreads = kVerifyWarps * 32;
 
 template <int D, int KV, int NM>
 static cudaError_t verify_one(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p, dim3 grid,
