@@ -237,14 +237,20 @@ pfkv_status make_plan(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_k
     if (e == cudaSuccess) e = sm_count(dev, &sms);
     if (e != cudaSuccess) return cuda_fail(e, "device query");
     const int units = num_seqs > 0 ? num_seqs * Hkv : 1;
-    const int target = sms * ctas_per_sm(dev, pl->cfg, pl->ncw, pl->tc, pl->nmax);
-    const int base = (target + units - 1) / units;
-    // bound the keys per CTA so ragged batches balance; the bound grows with
-    // the row count because every range costs an fp32 partial per row, and doubles
-    // for the tcgen05 kernel (one CTA per SM, with a fixed start-up and first-tile cost
-    // worth ~8 tiles: two waves of half-length ranges cost more than one wave)
+    const int occ = ctas_per_sm(dev, pl->cfg, pl->ncw, pl->tc, pl->nmax);
+    int base = (sms * occ + units - 1) / units;
+    // Long ranges at full occupancy: one CTA per SM with ranges twice as long measured faster
+    // (128K-key decode: 38 ranges 54 us, 76 ranges 58 us; with 4096 keys, 5 tiles per range,
+    // the three CTAs per SM stay ahead).
+    const bool long_ranges = !pl->tc && occ > 1 && tiles >= 24 * base;
+    if (long_ranges) base = (sms + units - 1) / units;
+    // Bound the keys per CTA so ragged batches balance (when sequences outnumber the SMs, each
+    // range is a unit of work of the wave); the bound grows with the row count because every
+    // range costs an fp32 partial per row, and doubles for the tcgen05 kernel (one CTA per
+    // SM, with a fixed start-up and first-tile cost worth ~8 tiles: two waves of half-length
+    // ranges cost more than one wave).
     const int max_keys = (pl->tc ? 2 : 1) * (R * 256 > 2048 ? R * 256 : 2048);
-    const int need = (max_seq_len + max_keys - 1) / max_keys;
+    const int need = (long_ranges && units < sms) ? 1 : (max_seq_len + max_keys - 1) / max_keys;
     const int k = base > 0 ? (need + base - 1) / base : 1;
     want = base * (k > 1 ? k : 1);
   }

@@ -5,10 +5,11 @@
 //   out = sum_s w_s o_s / sum_s w_s, lse = M + ln(sum_s w_s).
 //
 // One CTA of 8 warps per output row; the row's parts are spread over the
-// warps so that a row with many split ranges still costs about one memory
-// round trip. When launched after the decode kernel with programmatic
-// stream serialisation, the grid starts while the decode kernel drains and
-// waits (griddepcontrol.wait) before touching the partials.
+// warps, each warp keeping a running maximum, so that a row with up to 64
+// split ranges costs one memory round trip. When launched after the decode
+// kernel with programmatic stream serialisation, the grid starts while the
+// decode kernel drains and waits (griddepcontrol.wait) before touching the
+// partials.
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
@@ -23,14 +24,14 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(__half* __restrict__ out
                                                         const int32_t* __restrict__ seq_lens, int rows_per_seq,
                                                         int split_tokens, int len_cap) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // One CTA (8 warps) per row. Warp w takes parts w, w+8, ...; each lane owns
-  // D/32 consecutive output elements. The row maximum is reduced first (all
-  // part LSEs in one pass), every warp then issues the loads of up to kBatch
-  // of its parts before using any, and the 8 warp partial sums are added
-  // through shared memory.
+  // One CTA (8 warps) per row. Warp w takes parts w, w+8, ...; each lane owns D/32
+  // consecutive output elements. A warp issues the loads (LSE and output) of up to kBatch of
+  // its parts at once and keeps a running maximum with sums rescaled to it, so a row costs
+  // one memory round trip; the 8 warps' results are then rescaled to the row maximum and
+  // added through shared memory.
   constexpr int PER = D / 32;  // 4 or 8 floats per lane
   constexpr int kBatch = 8;
-  __shared__ float s_red[8];
+  __shared__ float s_m[8];
   __shared__ float s_w[8];
   __shared__ float4 s_acc[8][D / 4];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -44,67 +45,75 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(__half* __restrict__ out
   }
   const float* lp = lse_parts + static_cast<int64_t>(r) * num_parts;
   const float* op = o_parts + static_cast<int64_t>(r) * num_parts * D + lane * PER;
-  float M = -CUDART_INF_F;
-  for (int s = threadIdx.x; s < n; s += blockDim.x) M = fmaxf(M, lp[s]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  if (lane == 0) s_red[warp] = M;
-  __syncthreads();
-  M = s_red[0];
-#pragma unroll
-  for (int w = 1; w < 8; ++w) M = fmaxf(M, s_red[w]);
-
+  float Mw = -CUDART_INF_F, Ww = 0.f;  // this warp's running maximum and weight sum
   float acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-  float W = 0.f;
-  if (M != -CUDART_INF_F) {
-    for (int s0 = warp; s0 < n; s0 += 8 * kBatch) {
-      float4 v[kBatch][PER / 4];
-      float l[kBatch];
+  for (int s0 = warp; s0 < n; s0 += 8 * kBatch) {
+    float4 v[kBatch][PER / 4];
+    float l[kBatch];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int s = s0 + 8 * u;
-        if (s < n) {
-          l[u] = lp[s];
+    for (int u = 0; u < kBatch; ++u) {
+      const int s = s0 + 8 * u;
+      l[u] = -CUDART_INF_F;
+      if (s < n) {
+        l[u] = lp[s];
 #pragma unroll
-          for (int i = 0; i < PER / 4; ++i)
-            v[u][i] = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(s) * D + 4 * i);
-        }
+        for (int i = 0; i < PER / 4; ++i)
+          v[u][i] = *reinterpret_cast<const float4*>(op + static_cast<int64_t>(s) * D + 4 * i);
       }
+    }
+    float bm = -CUDART_INF_F;
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        if (s0 + 8 * u < n) {
-          const float w = (l[u] == -CUDART_INF_F) ? 0.f : expf(l[u] - M);
-          W += w;
+    for (int u = 0; u < kBatch; ++u) bm = fmaxf(bm, l[u]);
+    const float nm = fmaxf(Mw, bm);
+    if (nm == -CUDART_INF_F) continue;  // nothing visible yet (uniform across the warp)
+    const float sc = (Mw == -CUDART_INF_F) ? 0.f : expf(Mw - nm);
+    Ww *= sc;
 #pragma unroll
-          for (int i = 0; i < PER / 4; ++i) {
-            acc[4 * i + 0] += w * v[u][i].x;
-            acc[4 * i + 1] += w * v[u][i].y;
-            acc[4 * i + 2] += w * v[u][i].z;
-            acc[4 * i + 3] += w * v[u][i].w;
-          }
+    for (int i = 0; i < PER; ++i) acc[i] *= sc;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (s0 + 8 * u < n && l[u] != -CUDART_INF_F) {
+        const float w = expf(l[u] - nm);
+        Ww += w;
+#pragma unroll
+        for (int i = 0; i < PER / 4; ++i) {
+          acc[4 * i + 0] += w * v[u][i].x;
+          acc[4 * i + 1] += w * v[u][i].y;
+          acc[4 * i + 2] += w * v[u][i].z;
+          acc[4 * i + 3] += w * v[u][i].w;
         }
       }
     }
+    Mw = nm;
   }
 #pragma unroll
   for (int i = 0; i < PER / 4; ++i)
     s_acc[warp][lane * (PER / 4) + i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
-  if (lane == 0) s_w[warp] = W;
+  if (lane == 0) {
+    s_m[warp] = Mw;
+    s_w[warp] = Ww;
+  }
   __syncthreads();
-  // 256 threads finish D / 4 float4 outputs (D = 128: 32 threads, D = 256: 64 threads)
+  // D / 4 threads finish the float4 outputs (D = 128: 32 threads, D = 256: 64 threads)
   if (threadIdx.x < D / 4) {
+    float M = s_m[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) M = fmaxf(M, s_m[w]);
     float Wt = 0.f;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -CUDART_INF_F) {
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      Wt += s_w[w];
-      const float4 x = s_acc[w][threadIdx.x];
-      a.x += x.x;
-      a.y += x.y;
-      a.z += x.z;
-      a.w += x.w;
+      for (int w = 0; w < 8; ++w) {
+        const float f = (s_m[w] == -CUDART_INF_F) ? 0.f : expf(s_m[w] - M);
+        Wt += f * s_w[w];
+        const float4 x = s_acc[w][threadIdx.x];
+        a.x += f * x.x;
+        a.y += f * x.y;
+        a.z += f * x.z;
+        a.w += f * x.w;
+      }
     }
     const bool has = (M != -CUDART_INF_F) && (Wt > 0.f);
     const float inv = has ? 1.f / Wt : 0.f;
