@@ -232,7 +232,10 @@ class DeviceWorkload:
         self.splits, self.split_tokens = pf.pfkv_decode_plan(B, T, Hq, s.num_kv_heads, s.head_dim, s.page_size,
                                                              s.kv_dtype, self.max_seq_len, 0)
         self.has_append = case.slot_new.size > 0
-        self.launches_per_step = (1 if self.has_append else 0) + 1 + (1 if self.splits > 1 else 0)
+        # a split plan launches the merge kernel unless its ranges combine inside thread-block
+        # clusters, in which case the library asks for no workspace
+        merge = self.splits > 1 and ws > 0
+        self.launches_per_step = (1 if self.has_append else 0) + 1 + (1 if merge else 0)
 
     def append_step(self):
         s = self.case.spec

@@ -77,6 +77,16 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
   // launched with programmatic stream serialisation: wait for the preceding
   // grid (which may produce q, the cache or the tables) before any global read
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The producer warp fetches the block-table entries of the range's first 32 pages now, so
+  // that the load overlaps the sequence-length load (the range's first page does not depend
+  // on the length; entries stay inside the table row; they are validated once the length is
+  // known).
+  const int pfirst0 = (split * p.split_tokens) >> p.page_shift;
+  int pre_id = 0;
+  if ((threadIdx.x >> 5) == ncw) {
+    const int m = pfirst0 + (threadIdx.x & 31);
+    if (m < p.max_blocks) pre_id = p.block_table[static_cast<size_t>(b) * p.max_blocks + m];
+  }
   // sequence length, validated against what the block table can address
   int N = p.seq_lens[b];
   {
@@ -120,8 +130,19 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
       const int P = p.page_size;
       const int* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks;
       const int page_last = (t1 - 1) >> p.page_shift;
-      int chunk_base = -(1 << 30);  // first page index held by the lanes' ids (none yet)
+      // the lanes hold the ids of pages chunk_base .. chunk_base + 31 (prefetched above)
+      int chunk_base = pfirst0;
       int my_id = 0;
+      {
+        const int mine = chunk_base + lane;
+        if (mine <= page_last) {
+          my_id = pre_id;
+          if (static_cast<unsigned>(my_id) >= static_cast<unsigned>(p.num_blocks)) {
+            atomicOr(p.err, kDevErrBlockId);
+            my_id = 0;
+          }
+        }
+      }
       auto page_id = [&](int pidx) -> int {
         if (pidx < chunk_base || pidx >= chunk_base + 32) {
           chunk_base = pidx;
