@@ -482,11 +482,14 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
       const uint64_t q_desc = umma_desc_sw128(smem_u32(smem + S::OFF_Q));
       const uint64_t k_desc = umma_desc_sw128(smem_u32(smem + S::OFF_KRING));
       const uint64_t pt_desc = umma_desc_sw128(smem_u32(smem + S::OFF_PT));
-      // With one S^T buffer the order is fixed: S^T(0), then per tile i: S^T(i+1) (its K tile
-      // landed, S^T(i) read out by the softmax, which happens at the start of tile i), then
-      // O^T(i) (V^T(i) and P^T(i) written, at the end of tile i). Blocking waits wake as soon as
-      // the phase completes. Each parity wait is sound: this thread saw the previous phase of
-      // that barrier, and its next phase needs an MMA this thread has not issued yet.
+      // With one S^T buffer the issue order is fixed, and the tensor pipe executes in issue
+      // order: S^T(0), S^T(1), then per tile i, once P^T(i) and V^T(i) are written: S^T(i+2)
+      // (its K tile landed and the softmax read S^T(i+1) out, which it does right after
+      // finishing tile i), then O^T(i). S^T of the tile after next thus never queues behind a
+      // tile's 16 O^T MMAs; O^T(i) is only needed two tiles later (P^T and V^T are double
+      // buffered). Blocking waits wake as soon as the phase completes. Each parity wait is
+      // sound: this thread saw the previous phase of that barrier, and its next phase needs an
+      // MMA this thread has not issued yet.
       // (Issuing the O^T MMAs from a second warp was measured slower: that warp's sub-partition
       // also runs a V converter, which then fell behind.)
       bool ok = true;
@@ -506,16 +509,23 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
         tc_fence_after();
         issue_s(0);
       }
+      if (ok && ntiles > 1) {
+        ok = mbar_wait(&kfull[1 % NK], (1 / NK) & 1) && mbar_wait(s_free, 0);
+        if (ok) {
+          tc_fence_after();
+          issue_s(1);
+        }
+      }
       for (int on = 0; on < ntiles && ok; ++on) {
-        const int sn = on + 1;
+        ok = mbar_wait(&av_full[on % NAV], (on / NAV) & 1) && mbar_wait(&pt_full[on & 1], (on >> 1) & 1);
+        if (!ok) break;
+        const int sn = on + 2;
         if (sn < ntiles) {
           ok = mbar_wait(&kfull[sn % NK], (sn / NK) & 1) && mbar_wait(s_free, (sn - 1) & 1);
           if (!ok) break;
           tc_fence_after();
           issue_s(sn);
         }
-        ok = mbar_wait(&av_full[on % NAV], (on / NAV) & 1) && mbar_wait(&pt_full[on & 1], (on >> 1) & 1);
-        if (!ok) break;
         tc_fence_after();
         const uint64_t pt = pt_desc + static_cast<uint64_t>(((on & 1) * S::PT_BYTES) >> 4);
         const uint32_t av = tbase + S::COL_AV + (on % NAV) * S::AV_COLS;
