@@ -185,6 +185,15 @@ PFKV_API size_t pfkv_decode_workspace_bytes(int num_seqs, int num_q_tokens, int 
  * Supported: head_dim 128 or 256; page_size a power of two in [16, 2048];
  * 1 <= num_q_tokens <= 8; num_q_heads % num_kv_heads == 0 and
  * num_q_tokens * g <= 64.
+ *
+ * Arithmetic (within 2e-3 of the exact out and 1e-4 of the exact lse on
+ * unit-scale inputs): cache values are decoded exactly; logits are fp32
+ * sums; the softmax weights enter the PV product rounded to fp16, while their
+ * sums stay fp32. With an FP8 cache and more than 16 rows per KV head
+ * (num_q_tokens * g) the kernel runs on the 5th-generation tensor cores and
+ * Q enters them as three E4M3 terms per element (each row scaled by a power
+ * of two), whose sum equals the fp16 value to within half an E4M3 subnormal
+ * step of the scaled row.
  */
 PFKV_API pfkv_status pfkv_paged_attention_decode(void* out, float* lse, const void* q,
                                         const void* k_cache, const void* v_cache,
