@@ -5,8 +5,9 @@
 // exact grouped q8 verification over FP8 KV) form a real dense tile.
 //
 // One CTA = one (key range, KV head, sequence), 14 warps:
-//   warp 0      producer: TMA tile copies of 128-key FP8 K and V tiles into
-//               two shared-memory rings (same tensor maps as the decode kernel);
+//   warp 0      producers: TMA tile copies of 128-key FP8 K (lane 0) and V
+//               (lane 1) tiles into two shared-memory rings (same tensor maps
+//               as the decode kernel);
 //   warp 1      MMA issuer (one lane) and TMEM owner;
 //   warps 2-9   softmax: each thread owns one key of the tile (its TMEM lane)
 //               and half of the query rows; it pulls the key's logits from
@@ -371,40 +372,35 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
   bool alive = true;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- producer
-    if (ntiles > 0) {
-      if (lane == 0) {
-        prefetch_tensormap(&tmk);
-        prefetch_tensormap(&tmv);
-      }
+    // ---------------------------------------------------------------- producers (lanes 0 and 1)
+    // Lane 0 copies the K tiles, lane 1 the V tiles, each into its own ring and each sleeping
+    // in its own slot waits: the two divergent paths of the warp progress independently, so a
+    // V copy never waits behind a K slot (freed by the S^T MMAs) nor the reverse. Each lane
+    // reads the block-table entries it needs itself (a page id is reused while its page lasts).
+    if (ntiles > 0 && lane < 2) {
+      const int which = lane;  // 0: K, 1: V
+      const CUtensorMap* map = which == 0 ? &tmk : &tmv;
+      prefetch_tensormap(map);
+      uint64_t* fullb = which == 0 ? kfull : vfull;
+      uint64_t* emptyb = which == 0 ? kempty : vempty;
+      const int depth = which == 0 ? NK : NV;
+      unsigned char* ring = smem + (which == 0 ? S::OFF_KRING : S::OFF_VRING);
       const int P = p.page_size;
       const int* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks;
-      const int page_last = (t1 - 1) >> p.page_shift;
-      // 32 lanes fetch 32 consecutive page ids at a time; lane 0 reads them by shuffle
-      int chunk_base = -(1 << 30);
-      int my_id = 0;
+      int cur_page = -1, cur_id = 0;
       auto page_id = [&](int pidx) -> int {
-        if (pidx < chunk_base || pidx >= chunk_base + 32) {
-          chunk_base = pidx;
-          const int mine = chunk_base + lane;
-          my_id = 0;
-          if (mine <= page_last) {
-            my_id = bt[mine];
-            if (static_cast<unsigned>(my_id) >= static_cast<unsigned>(p.num_blocks)) {
-              atomicOr(p.err, kDevErrBlockId);
-              my_id = 0;
-            }
+        if (pidx != cur_page) {
+          cur_page = pidx;
+          cur_id = bt[pidx];
+          if (static_cast<unsigned>(cur_id) >= static_cast<unsigned>(p.num_blocks)) {
+            atomicOr(p.err, kDevErrBlockId);
+            cur_id = 0;
           }
         }
-        return __shfl_sync(0xffffffffu, my_id, pidx - chunk_base);
+        return cur_id;
       };
-      auto wait_slot = [&](uint64_t* bar, int it, int depth) -> bool {
-        if (it < depth) return true;
-        bool got = true;
-        if (lane == 0) got = mbar_wait(&bar[it % depth], ((it / depth) - 1) & 1);
-        return __shfl_sync(0xffffffffu, got, 0);
-      };
-      for (int it = 0; it < ntiles && alive; ++it) {
+      int it = 0;
+      for (; it < ntiles; ++it) {
         const int tile_start = t0 + it * KT;
         const int valid = min(KT, t1 - tile_start);
         // rows of the tile's 64-row boxes (P >= 64) or pages (P < 64); at most 8
@@ -426,51 +422,42 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
 #pragma unroll
           for (int pg = 0; pg < 8; ++pg) {
             rows[pg] = 0;
-            if (pg < nbox_rows) rows[pg] = (page_id(pfirst + pg) * p.num_kv_heads + kvh) * P;
+            if (pg < nbox_rows) {
+              int id = bt[pfirst + pg];  // independent loads: one round trip per tile
+              if (static_cast<unsigned>(id) >= static_cast<unsigned>(p.num_blocks)) {
+                atomicOr(p.err, kDevErrBlockId);
+                id = 0;
+              }
+              rows[pg] = (id * p.num_kv_heads + kvh) * P;
+            }
           }
         }
-        const uint32_t bytes = NBOX * nbox_rows * box_rows * kBoxBytes;
-        // K tile, then V tile, each into its own ring
-        for (int which = 0; which < 2; ++which) {
-          uint64_t* fullb = which == 0 ? kfull : vfull;
-          uint64_t* emptyb = which == 0 ? kempty : vempty;
-          const int depth = which == 0 ? NK : NV;
-          if (!wait_slot(emptyb, it, depth)) {
-            if (lane == 0) atomicOr(p.err, kDevErrTimeout);
-            alive = false;
-            break;
-          }
-          unsigned char* dst = smem + (which == 0 ? S::OFF_KRING : S::OFF_VRING) + (it % depth) * S::KV_TILE;
-          const CUtensorMap* map = which == 0 ? &tmk : &tmv;
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&fullb[it % depth], bytes);
+        // slot of tile it-depth released (its previous phase, of tile it-2*depth, was waited
+        // for by this lane; the next one needs this lane's own copy of tile it)
+        if (it >= depth && !mbar_wait(&emptyb[it % depth], ((it / depth) - 1) & 1)) {
+          atomicOr(p.err, kDevErrTimeout);
+          break;
+        }
+        unsigned char* dst = ring + (it % depth) * S::KV_TILE;
+        mbar_arrive_expect_tx(&fullb[it % depth], NBOX * nbox_rows * box_rows * kBoxBytes);
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              if (r < nbox_rows) {
+        for (int r = 0; r < 8; ++r) {
+          if (r < nbox_rows) {
 #pragma unroll
-                for (int bx = 0; bx < NBOX; ++bx)
-                  tma_load_2d(dst + bx * S::SUB + r * box_rows * kBoxBytes, map, &fullb[it % depth], bx * kBoxBytes,
-                              rows[r]);
-              }
-            }
+            for (int bx = 0; bx < NBOX; ++bx)
+              tma_load_2d(dst + bx * S::SUB + r * box_rows * kBoxBytes, map, &fullb[it % depth], bx * kBoxBytes,
+                          rows[r]);
           }
         }
       }
       // do not leave while copies may still land in this CTA's shared memory
-      if (lane == 0) {
-        for (int it = max(0, ntiles - NK); it < ntiles; ++it)
-          if (!mbar_wait(&kfull[it % NK], (it / NK) & 1)) {
-            atomicOr(p.err, kDevErrTimeout);
-            break;
-          }
-        for (int it = max(0, ntiles - NV); it < ntiles; ++it)
-          if (!mbar_wait(&vfull[it % NV], (it / NV) & 1)) {
-            atomicOr(p.err, kDevErrTimeout);
-            break;
-          }
-      }
-      __syncwarp();
+      for (int jt = max(0, it - depth); jt < it; ++jt)
+        if (!mbar_wait(&fullb[jt % depth], (jt / depth) & 1)) {
+          atomicOr(p.err, kDevErrTimeout);
+          break;
+        }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && ntiles > 0) {
