@@ -68,7 +68,9 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
   constexpr int ROWS_W = 8 * NT;  // query rows per consumer warp
 
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1 KB-aligned base, formed by pointer arithmetic on the shared array so that every pointer
+  // derived from it stays a shared-memory pointer (32-bit shared loads and stores)
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int ncw = p.nrg * p.nts;

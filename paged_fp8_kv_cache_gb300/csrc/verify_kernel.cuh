@@ -85,9 +85,10 @@ struct VerifyShape {
   static_assert(COL_AV + NAV * AV_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(NQ <= 256, "MMA N");
   static_assert(HN % 8 == 0, "softmax rows come in TMEM loads of 8 columns");
-  // misc: m_ref, alpha, sc2r, rscale, wred[4], lsum[4] (NMAX floats each), out_row (NMAX ints),
-  // vote flags, TMEM slot, barriers
-  static constexpr int MISC_BYTES = 13 * NMAX * 4 + 64 + 32 * 8;
+  // misc: m_ref, alpha, sc2r, rscale, wred[4], lsum[4], m_use, thr, dx (NMAX floats each),
+  // out_row (NMAX ints), vote flags, TMEM slot, barriers
+  static constexpr int MISC_WORDS = 16 * NMAX;
+  static constexpr int MISC_BYTES = MISC_WORDS * 4 + 64 + 32 * 8;
   static constexpr int kSmemLimit = 227 * 1024;
   static constexpr int FIT = (kSmemLimit - 1024 - Q_BYTES - 2 * PT_BYTES - MISC_BYTES) / KV_TILE;
   static constexpr int NK = FIT / 2 > 4 ? 4 : FIT / 2;
@@ -224,7 +225,9 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
   using S = VerifyShape<D, NMAX_>;
   constexpr int KT = S::KT, NBOX = S::NBOX, NK = S::NK, NV = S::NV, NMAX = S::NMAX, MT = S::MT, HN = S::HN;
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1 KB-aligned base, formed by pointer arithmetic on the shared array so that every pointer
+  // derived from it stays a shared-memory pointer (32-bit shared loads and stores)
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int R = p.T * p.G;
@@ -251,10 +254,15 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
   float* rscale = sc2r + NMAX;                                   // [NMAX] output scale v_scale / L
   float* wred = rscale + NMAX;                                   // [4][NMAX] per-quadrant maxima
   float* lsum = wred + 4 * NMAX;                                 // [4][NMAX] per-quadrant row sums
-  int* out_row = reinterpret_cast<int*>(lsum + 4 * NMAX);        // [NMAX] output row of row r
+  // the reference as the logits use it: m_ref, or 0 while a row has none (kNoRef); and the
+  // threshold above which a logit forces an update: kRescaleLog2, or -inf while it has none
+  float* m_use = lsum + 4 * NMAX;                                // [NMAX]
+  float* thr = m_use + NMAX;                                     // [NMAX]
+  float* dx_s = thr + NMAX;                                      // [NMAX] old m_use - new m_use
+  int* out_row = reinterpret_cast<int*>(dx_s + NMAX);            // [NMAX] output row of row r
   int* flag = out_row + NMAX;                                    // [3] rescale votes
   uint32_t* tslot = reinterpret_cast<uint32_t*>(flag + 4);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_MISC + 13 * NMAX * 4 + 64);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_MISC + S::MISC_WORDS * 4 + 64);
   uint64_t* kfull = bars;              // [NK] producer -> MMA (K tile landed)
   uint64_t* kempty = kfull + NK;       // [NK] MMA commit: S^T MMAs done reading the K tile
   uint64_t* vfull = kempty + NK;       // [NV] producer -> V converter
@@ -361,7 +369,11 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
         }
       }
     }
-    for (int i = tid; i < NMAX; i += blockDim.x) m_ref[i] = kNoRef;
+    for (int i = tid; i < NMAX; i += blockDim.x) {
+      m_ref[i] = kNoRef;
+      m_use[i] = 0.f;
+      thr[i] = -CUDART_INF_F;
+    }
     if (tid == 0) flag[0] = flag[1] = flag[2] = 0;
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -632,10 +644,10 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
       m[6] = c.z;
       m[7] = c.w;
     };
-    // 2^(s - m) for x = s - m (base-2 units), capped so that a logit that outgrew its reference
-    // stays finite (the tile is then redone). A row without a reference yet has m = kNoRef, so x
-    // is 1e30 for a visible key, p = 2^15 and x > kRescaleLog2: such a tile always takes the
-    // update, whose factor for that row is 2^(kNoRef - m) = 0, and is redone.
+    // 2^x for x = s - m_use (base-2 units), capped so that a logit that outgrew its reference
+    // stays finite (the tile is then redone). A row without a reference yet (m_use = 0) has the
+    // threshold -inf, so any visible key of it forces the update, whose factor for that row is
+    // 2^(kNoRef - m) = 0; the tile is then redone against the new reference.
     auto pexp = [](float x) -> float { return fast_exp2(fminf(x, 15.f)); };
     for (int it = 0; it < ntiles && alive; ++it) {
       const int sb = it & 1;
@@ -650,29 +662,39 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
       // row r sees this key iff r / G >= kp - (N - T), i.e. r >= G * (kp - (N - T))
       const int rmin = p.G * (kp - tlim_base);
       const bool all_vis = (tile_start + KT <= t1) && (tile_start + KT - 1 <= tlim_base);  // CTA-uniform
-      // this key's logits of rows rbase .. rbase+HN-1 (sum of the three Q-term columns), in
-      // base-2 units, -inf where masked; then the S^T buffer goes back to the MMA warp
-      // and whether any of them exceeds its row's reference by more than kRescaleLog2
-      float s2[HN];
+      // this key's logits of rows rbase .. rbase+HN-1 (sum of the three Q-term columns) less
+      // the rows' references, x = s - m_use in base-2 units, -inf where masked; then the S^T
+      // buffer goes back to the MMA warp. And whether any x exceeds its row's threshold.
+      float x[HN];
       bool exceed = false;
 #pragma unroll
       for (int c = 0; c < HN; c += 8) {
         uint32_t v0[8], v1[8], v2[8];
-        float sc[8], m[8];
+        float sc[8], mu[8], th[8];
         const uint32_t col = tq + S::COL_S + rbase + c;
         tmem_ld8(col, v0);
         tmem_ld8(col + NMAX, v1);
         tmem_ld8(col + 2 * NMAX, v2);
         load8(sc2r + rbase + c, sc);
-        load8(m_ref + rbase + c, m);
+        load8(m_use + rbase + c, mu);
+        load8(thr + rbase + c, th);
         tmem_wait_ld();
+        if (all_vis) {  // CTA-uniform: every row sees every key of the tile
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = rbase + c + j;
-          const bool vis = all_vis || (in_range && (r >= R || r >= rmin));
-          const float raw = (__uint_as_float(v0[j]) + __uint_as_float(v1[j])) + __uint_as_float(v2[j]);
-          s2[c + j] = vis ? raw * sc[j] : -CUDART_INF_F;
-          exceed |= (s2[c + j] - m[j] > kRescaleLog2);
+          for (int j = 0; j < 8; ++j) {
+            const float raw = (__uint_as_float(v0[j]) + __uint_as_float(v1[j])) + __uint_as_float(v2[j]);
+            x[c + j] = fmaf(raw, sc[j], -mu[j]);
+            exceed |= x[c + j] > th[j];
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int r = rbase + c + j;
+            const bool vis = in_range && (r >= R || r >= rmin);
+            const float raw = (__uint_as_float(v0[j]) + __uint_as_float(v1[j])) + __uint_as_float(v2[j]);
+            x[c + j] = vis ? fmaf(raw, sc[j], -mu[j]) : -CUDART_INF_F;
+            exceed |= x[c + j] > th[j];
+          }
         }
       }
       tc_fence_before();
@@ -705,34 +727,44 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
           // terms (same formula, same values) taken back out of the row sums
 #pragma unroll
           for (int c = 0; c < HN; c += 8) {
-            float m[8];
-            load8(m_ref + rbase + c, m);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              float mx = s2[c + j];
+              float mx = x[c + j];
 #pragma unroll
               for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
               if (lane == 0) wred[q * NMAX + rbase + c + j] = mx;
-              if (did_pass) l_part[c + j] -= pexp(s2[c + j] - m[j]);
+              if (did_pass) l_part[c + j] -= pexp(x[c + j]);
             }
           }
           swg_sync();
           if (sidx < NMAX) {
             const int r = sidx;
-            const float mt = fmaxf(fmaxf(wred[r], wred[NMAX + r]), fmaxf(wred[2 * NMAX + r], wred[3 * NMAX + r]));
+            const float mu_old = m_use[r];
+            // the tile's row maximum of s (x + m_use: -inf if every key is masked)
+            const float mt =
+                fmaxf(fmaxf(wred[r], wred[NMAX + r]), fmaxf(wred[2 * NMAX + r], wred[3 * NMAX + r])) + mu_old;
             const float mo = m_ref[r];
             const float mn = fmaxf(mo, mt);
             // the reference only moves up; rows with nothing visible so far keep kNoRef
+            const bool none = !(mn > kNoRef);
+            const float mu_new = none ? 0.f : mn;
             alpha_s[r] = fast_exp2(mo - mn);
             m_ref[r] = mn;
+            m_use[r] = mu_new;
+            thr[r] = none ? -CUDART_INF_F : kRescaleLog2;
+            dx_s[r] = mu_old - mu_new;
           }
           swg_sync();
 #pragma unroll
           for (int c = 0; c < HN; c += 8) {
-            float a[8];
+            float a[8], d[8];
             load8(alpha_s + rbase + c, a);
+            load8(dx_s + rbase + c, d);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) l_part[c + j] *= a[j];
+            for (int j = 0; j < 8; ++j) {
+              l_part[c + j] *= a[j];
+              x[c + j] += d[j];  // against the new reference (-inf stays -inf)
+            }
           }
           if (it > 0) {
             // rescale the O^T columns once the previous tile's MMAs are done (sound: this
@@ -760,12 +792,9 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
         // one pass: P^T and the row sums against the current references
 #pragma unroll
         for (int c = 0; c < HN; c += 8) {
-          float m[8];
-          load8(m_ref + rbase + c, m);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float x = s2[c + j] - m[j];
-            const float pr = pexp(x);
+            const float pr = pexp(x[c + j]);
             l_part[c + j] += pr;
             *reinterpret_cast<__half*>(pt + sw128_elem(rbase + c + j, kk)) = __float2half_rn(pr);
           }
