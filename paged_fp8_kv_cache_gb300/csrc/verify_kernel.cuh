@@ -181,6 +181,10 @@ __device__ __forceinline__ int sw128_elem(int row, int k) {
   return row * 128 + ((((k >> 3) ^ row) & 7) << 4) + ((k & 7) << 1);
 }
 
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint32_t low16) {
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(static_cast<unsigned short>(low16)) : "memory");
+}
+
 // two FP8 codes (low byte -> low half) to an fp16 pair
 template <int KV>
 __device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t two) {
@@ -620,6 +624,15 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
     const int key_lane = 32 * q + lane;
     const int sidx = sw * 32 + lane;   // 0..255: the row owned in the per-row steps
     const uint32_t tq = tbase + (static_cast<uint32_t>(32 * q) << 16);
+    // shared addresses of this thread's P^T element (its key) in rows rbase + 8i + j of buffer 0:
+    // rbase and 8i are multiples of 8, so row & 7 = j and the swizzle depends on j alone
+    uint32_t pta[8];
+    {
+      const int kk = key_lane & 63;
+      const uint32_t pt0 = smem_u32(smem + S::OFF_PT + (key_lane >> 6) * NMAX * 128);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) pta[j] = pt0 + static_cast<uint32_t>(sw128_elem(rbase + j, kk));
+    }
     uint32_t swg_phase = 0;
     // the softmax warps meet; a wait that runs out marks the CTA's work as failed
     auto swg_sync = [&]() {
@@ -716,8 +729,7 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
         alive = false;
         break;
       }
-      unsigned char* pt = smem + S::OFF_PT + sb * S::PT_BYTES + (key_lane >> 6) * NMAX * 128;
-      const int kk = key_lane & 63;
+      const uint32_t ptb = sb * S::PT_BYTES;  // P^T buffer sb
       bool update = (it == 0);  // the first tile has no references yet
       bool did_pass = false;
 #pragma unroll 1
@@ -793,10 +805,14 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
 #pragma unroll
         for (int c = 0; c < HN; c += 8) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float pr = pexp(x[c + j]);
-            l_part[c + j] += pr;
-            *reinterpret_cast<__half*>(pt + sw128_elem(rbase + c + j, kk)) = __float2half_rn(pr);
+          for (int j = 0; j < 8; j += 2) {
+            const float p0 = pexp(x[c + j]), p1 = pexp(x[c + j + 1]);
+            l_part[c + j] += p0;
+            l_part[c + j + 1] += p1;
+            const __half2 h = __floats2half2_rn(p0, p1);
+            const uint32_t hw = *reinterpret_cast<const uint32_t*>(&h);
+            st_shared_u16(pta[j] + ptb + c * 128, hw);
+            st_shared_u16(pta[j + 1] + ptb + c * 128, hw >> 16);
           }
         }
         did_pass = true;
