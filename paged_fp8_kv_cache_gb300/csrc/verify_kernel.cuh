@@ -181,6 +181,11 @@ __device__ __forceinline__ int sw128_elem(int row, int k) {
   return row * 128 + ((((k >> 3) ^ row) & 7) << 4) + ((k & 7) << 1);
 }
 
+template <bool B>
+struct BoolTag {
+  static constexpr bool value = B;
+};
+
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint32_t low16) {
   asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(static_cast<unsigned short>(low16)) : "memory");
 }
@@ -572,40 +577,49 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
       const unsigned char* Vs = smem + S::OFF_VRING + s * S::KV_TILE;
       const uint32_t av = tq + S::COL_AV + (it % S::NAV) * S::AV_COLS;
       const int valid = min(KT, t1 - (t0 + it * KT));
-      const bool tail = valid < KT;
+      // a full tile and the range's last, partial one take separate copies of the loop, so that
+      // the full tiles carry no per-key range checks
+      auto convert_tile = [&](auto tail_tag) {
+        constexpr bool kTail = decltype(tail_tag)::value;
 #pragma unroll 1
-      for (int k0 = 0; k0 < KT; k0 += 32) {
-        const unsigned char* vrow = Vs + k0 * kBoxBytes;  // rows k0.. of the tile (k0 % 8 == 0)
-        uint32_t v0[16], v1[16];
+        for (int k0 = 0; k0 < KT; k0 += 32) {
+          const unsigned char* vrow = Vs + k0 * kBoxBytes;  // rows k0.. of the tile (k0 % 8 == 0)
+          uint32_t v0[16], v1[16];
 #pragma unroll
-        for (int kk = 0; kk < 32; kk += 2) {
-          const int oa = voff[kk & 7] + ((kk >> 3) << 10);
-          const int ob = voff[(kk + 1) & 7] + ((kk >> 3) << 10);
-          uint32_t wa, wb;
-          if constexpr (D == 256) {
-            wa = *reinterpret_cast<const uint16_t*>(vrow + oa);  // dims 2L, 2L+1 of key k0+kk
-            wb = *reinterpret_cast<const uint16_t*>(vrow + ob);
-          } else {
-            wa = vrow[oa];
-            wb = vrow[ob];
+          for (int kk = 0; kk < 32; kk += 2) {
+            const int oa = voff[kk & 7] + ((kk >> 3) << 10);
+            const int ob = voff[(kk + 1) & 7] + ((kk >> 3) << 10);
+            uint32_t wa, wb;
+            if constexpr (D == 256) {
+              wa = *reinterpret_cast<const uint16_t*>(vrow + oa);  // dims 2L, 2L+1 of key k0+kk
+              wb = *reinterpret_cast<const uint16_t*>(vrow + ob);
+            } else {
+              wa = vrow[oa];
+              wb = vrow[ob];
+            }
+            if constexpr (kTail) {  // stale bytes past the range end must not reach the MMA
+              if (k0 + kk >= valid) wa = 0u;
+              if (k0 + kk + 1 >= valid) wb = 0u;
+            }
+            if constexpr (KV == kKvE5m2 && D == 256) {
+              // an E5M2 code is the high byte of the fp16 with the same value: the fp16 pairs
+              // (key k, key k+1) of dims 2L and 2L+1 are byte moves, bytes 2-3 of wa being zero
+              v0[kk >> 1] = __byte_perm(wa, wb, 0x4202);  // [0, a.b0, 0, b.b0]
+              v1[kk >> 1] = __byte_perm(wa, wb, 0x5212);  // [0, a.b1, 0, b.b1]
+            } else {
+              const uint32_t X = __byte_perm(wa, wb, 0x5140);  // [a.b0, b.b0, a.b1, b.b1]
+              v0[kk >> 1] = fp8x2_to_f16x2<KV>(X);
+              v1[kk >> 1] = fp8x2_to_f16x2<KV>(X >> 16);
+            }
           }
-          if (tail) {  // stale bytes past the range end must not reach the MMA
-            if (k0 + kk >= valid) wa = 0u;
-            if (k0 + kk + 1 >= valid) wb = 0u;
-          }
-          if constexpr (KV == kKvE5m2 && D == 256) {
-            // an E5M2 code is the high byte of the fp16 with the same value: the fp16 pairs
-            // (key k, key k+1) of dims 2L and 2L+1 are byte moves, bytes 2-3 of wa being zero
-            v0[kk >> 1] = __byte_perm(wa, wb, 0x4202);  // [0, a.b0, 0, b.b0]
-            v1[kk >> 1] = __byte_perm(wa, wb, 0x5212);  // [0, a.b1, 0, b.b1]
-          } else {
-            const uint32_t X = __byte_perm(wa, wb, 0x5140);  // [a.b0, b.b0, a.b1, b.b1]
-            v0[kk >> 1] = fp8x2_to_f16x2<KV>(X);
-            v1[kk >> 1] = fp8x2_to_f16x2<KV>(X >> 16);
-          }
+          tmem_st16(av + (k0 >> 1), v0);
+          if constexpr (MT == 2) tmem_st16(av + KT / 2 + (k0 >> 1), v1);
         }
-        tmem_st16(av + (k0 >> 1), v0);
-        if constexpr (MT == 2) tmem_st16(av + KT / 2 + (k0 >> 1), v1);
+      };
+      if (valid < KT) {
+        convert_tile(BoolTag<true>{});
+      } else {
+        convert_tile(BoolTag<false>{});
       }
       tmem_wait_st();
       tc_fence_before();
