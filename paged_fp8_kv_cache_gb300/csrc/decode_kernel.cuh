@@ -531,29 +531,41 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
   }
   asm volatile("barrier.sync 1, %0;" ::"r"(ncw * 32) : "memory");
 
-  // each consumer thread finishes (row, 4 consecutive dims) items
+  // each consumer thread finishes (row, 4 consecutive dims) items; the token slices of an item
+  // (p.nts of them: 2 or 4) are loaded together, so an item costs one shared-memory round trip
   const int rows_cta = min(R, p.nrg * ROWS_W);
   const bool final_out = (nsplit_b == 1);
-  const int items = rows_cta * (D / 4);
+  const int nts = p.nts;
+  constexpr int QD = D / 4;
+  const int items = rows_cta * QD;
   for (int idx = threadIdx.x; idx < items; idx += ncw * 32) {
-    const int r = idx / (D / 4);
-    const int d = (idx - r * (D / 4)) * 4;
+    const int r = idx / QD;
+    const int d = (idx - r * QD) * 4;
     const int rgr = r / ROWS_W, rr = r - rgr * ROWS_W;
-    float M = -CUDART_INF_F;
-    for (int t = 0; t < p.nts; ++t) M = fmaxf(M, ml_buf[(rgr * p.nts + t) * ROWS_W + rr].x);
+    float2 ml[4];
+    float4 v[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      ml[t] = make_float2(-CUDART_INF_F, 0.f);
+      v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < nts) {
+        const int wi = rgr * nts + t;
+        ml[t] = ml_buf[wi * ROWS_W + rr];
+        v[t] = *reinterpret_cast<const float4*>(obuf + (static_cast<size_t>(wi) * ROWS_W + rr) * D + d);
+      }
+    }
+    const float M = fmaxf(fmaxf(ml[0].x, ml[1].x), fmaxf(ml[2].x, ml[3].x));
     float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -CUDART_INF_F) {
-      for (int t = 0; t < p.nts; ++t) {
-        const int wi = rgr * p.nts + t;
-        const float2 ml = ml_buf[wi * ROWS_W + rr];
-        const float w = (ml.x == -CUDART_INF_F) ? 0.f : fast_exp2(ml.x - M);
-        L += w * ml.y;
-        const float4 v = *reinterpret_cast<const float4*>(obuf + (static_cast<size_t>(wi) * ROWS_W + rr) * D + d);
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {  // slices past nts have weight 0
+        const float w = (ml[t].x == -CUDART_INF_F) ? 0.f : fast_exp2(ml[t].x - M);
+        L += w * ml[t].y;
+        acc.x += w * v[t].x;
+        acc.y += w * v[t].y;
+        acc.z += w * v[t].z;
+        acc.w += w * v[t].w;
       }
     }
     const bool has = (M != -CUDART_INF_F) && (L > 0.f);
