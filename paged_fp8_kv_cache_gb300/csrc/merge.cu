@@ -23,7 +23,6 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(__half* __restrict__ out
                                                         const float* __restrict__ lse_parts, int rows, int num_parts,
                                                         const int32_t* __restrict__ seq_lens, int rows_per_seq,
                                                         int split_tokens, int len_cap) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   // One CTA (8 warps) per row. Warp w takes parts w, w+8, ...; each lane owns D/32
   // consecutive output elements. A warp issues the loads (LSE and output) of up to kBatch of
   // its parts at once and keeps a running maximum with sums rescaled to it, so a row costs
@@ -38,11 +37,15 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(__half* __restrict__ out
   const int r = blockIdx.x;
   int n = num_parts;
   if (seq_lens != nullptr) {
+    // The sequence lengths are read before this grid's dependency wait: they are an input of
+    // the decode call, complete before the decode kernel ran, and this grid starts only once
+    // every CTA of the decode kernel has passed its own wait (the partials are not).
     int len = seq_lens[r / rows_per_seq];
     len = len < 0 ? 0 : (len > len_cap ? len_cap : len);
     n = len > 0 ? (len + split_tokens - 1) / split_tokens : 1;
     if (n <= 1) return;  // written directly by the decode kernel (uniform across the CTA)
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const float* lp = lse_parts + static_cast<int64_t>(r) * num_parts;
   const float* op = o_parts + static_cast<int64_t>(r) * num_parts * D + lane * PER;
   float Mw = -CUDART_INF_F, Ww = 0.f;  // this warp's running maximum and weight sum
