@@ -531,61 +531,129 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
   }
   asm volatile("barrier.sync 1, %0;" ::"r"(ncw * 32) : "memory");
 
-  // each consumer thread finishes (row, 4 consecutive dims) items; the token slices of an item
-  // (p.nts of them: 2 or 4) are loaded together, so an item costs one shared-memory round trip
-  const int rows_cta = min(R, p.nrg * ROWS_W);
+  const int rows_cta = min(R, p.nrg * ROWS_W);  // at most 64 (4 row groups of 16)
   const bool final_out = (nsplit_b == 1);
-  const int nts = p.nts;
+  const int nts = p.nts;  // 2 or 4
   constexpr int QD = D / 4;
-  const int items = rows_cta * QD;
+  const int items = rows_cta * QD;  // (row, 4 consecutive dims) items
+  if (items <= ncw * 32) {
+    // At most one item per consumer thread: each thread combines its item's slices itself
+    // (the slices of an item are loaded together: one shared-memory round trip).
+    const int idx = threadIdx.x;
+    if (idx < items) {
+      const int r = idx / QD;
+      const int d = (idx - r * QD) * 4;
+      const int rgr = r / ROWS_W, rr = r - rgr * ROWS_W;
+      float2 ml[4];
+      float4 v[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        ml[t] = make_float2(-CUDART_INF_F, 0.f);
+        v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < nts) {
+          const int wi = rgr * nts + t;
+          ml[t] = ml_buf[wi * ROWS_W + rr];
+          v[t] = *reinterpret_cast<const float4*>(obuf + (static_cast<size_t>(wi) * ROWS_W + rr) * D + d);
+        }
+      }
+      const float M = fmaxf(fmaxf(ml[0].x, ml[1].x), fmaxf(ml[2].x, ml[3].x));
+      float L = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (M != -CUDART_INF_F) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {  // slices past nts have weight 0
+          const float w = (ml[t].x == -CUDART_INF_F) ? 0.f : fast_exp2(ml[t].x - M);
+          L += w * ml[t].y;
+          acc.x += w * v[t].x;
+          acc.y += w * v[t].y;
+          acc.z += w * v[t].z;
+          acc.w += w * v[t].w;
+        }
+      }
+      const bool has = (M != -CUDART_INF_F) && (L > 0.f);
+      const float inv = has ? vscale / L : 0.f;
+      const int t = r / p.G, j = r - t * p.G;
+      const size_t grow = (static_cast<size_t>(b) * p.T + t) * p.num_q_heads + kvh * p.G + j;
+      // natural-log LSE from base-2 running values
+      const float lse_val = has ? (M + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
+      if (final_out) {
+        __half2 h01 = __floats2half2_rn(acc.x * inv, acc.y * inv);
+        __half2 h23 = __floats2half2_rn(acc.z * inv, acc.w * inv);
+        uint2 packed;
+        packed.x = *reinterpret_cast<uint32_t*>(&h01);
+        packed.y = *reinterpret_cast<uint32_t*>(&h23);
+        *reinterpret_cast<uint2*>(p.out + grow * D + d) = packed;
+        if (d == 0) p.lse[grow] = lse_val;
+      } else {
+        float* dst = p.o_part + (grow * p.num_splits + split) * D + d;
+        *reinterpret_cast<float4*>(dst) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (d == 0) p.lse_part[grow * p.num_splits + split] = lse_val;
+      }
+    }
+    return;
+  }
+  // Several items per thread (e.g. 6 rows of 256 dims over 4 warps): first, per row (one thread
+  // each), the slices' weights 2^(m_t - M) folded with v_scale / L into four coefficients, the
+  // row's LSE and the offset of its output row; then every item is a 4-term weighted sum of the
+  // slices, with no per-item chain of exponentials, division and logarithm.
+  __shared__ float4 s_coef[64];
+  __shared__ long long s_orow[64];
+  if (threadIdx.x < rows_cta) {
+    const int r = threadIdx.x;
+    const int rgr = r / ROWS_W, rr = r - rgr * ROWS_W;
+    float2 ml[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) ml[t] = t < nts ? ml_buf[(rgr * nts + t) * ROWS_W + rr] : make_float2(-CUDART_INF_F, 0.f);
+    const float M = fmaxf(fmaxf(ml[0].x, ml[1].x), fmaxf(ml[2].x, ml[3].x));
+    float w[4];
+    float L = 0.f;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {  // slices past nts, and empty ones, have weight 0
+      w[t] = (ml[t].x == -CUDART_INF_F) ? 0.f : fast_exp2(ml[t].x - M);
+      L += w[t] * ml[t].y;
+    }
+    const bool has = (M != -CUDART_INF_F) && (L > 0.f);
+    const float inv = has ? vscale / L : 0.f;
+    s_coef[r] = make_float4(w[0] * inv, w[1] * inv, w[2] * inv, w[3] * inv);
+    const int t = r / p.G, j = r - t * p.G;
+    const long long grow = (static_cast<long long>(b) * p.T + t) * p.num_q_heads + kvh * p.G + j;
+    const float lse_val = has ? (M + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
+    if (final_out) {
+      s_orow[r] = grow * D;
+      p.lse[grow] = lse_val;
+    } else {
+      s_orow[r] = (grow * p.num_splits + split) * D;
+      p.lse_part[grow * p.num_splits + split] = lse_val;
+    }
+  }
+  asm volatile("barrier.sync 1, %0;" ::"r"(ncw * 32) : "memory");
   for (int idx = threadIdx.x; idx < items; idx += ncw * 32) {
     const int r = idx / QD;
     const int d = (idx - r * QD) * 4;
     const int rgr = r / ROWS_W, rr = r - rgr * ROWS_W;
-    float2 ml[4];
-    float4 v[4];
+    const float4 cf = s_coef[r];
+    const float cw[4] = {cf.x, cf.y, cf.z, cf.w};
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      ml[t] = make_float2(-CUDART_INF_F, 0.f);
-      v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (t < nts) {
-        const int wi = rgr * nts + t;
-        ml[t] = ml_buf[wi * ROWS_W + rr];
-        v[t] = *reinterpret_cast<const float4*>(obuf + (static_cast<size_t>(wi) * ROWS_W + rr) * D + d);
+        const float4 v = *reinterpret_cast<const float4*>(obuf + (static_cast<size_t>(rgr * nts + t) * ROWS_W + rr) * D + d);
+        acc.x += cw[t] * v.x;
+        acc.y += cw[t] * v.y;
+        acc.z += cw[t] * v.z;
+        acc.w += cw[t] * v.w;
       }
     }
-    const float M = fmaxf(fmaxf(ml[0].x, ml[1].x), fmaxf(ml[2].x, ml[3].x));
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -CUDART_INF_F) {
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {  // slices past nts have weight 0
-        const float w = (ml[t].x == -CUDART_INF_F) ? 0.f : fast_exp2(ml[t].x - M);
-        L += w * ml[t].y;
-        acc.x += w * v[t].x;
-        acc.y += w * v[t].y;
-        acc.z += w * v[t].z;
-        acc.w += w * v[t].w;
-      }
-    }
-    const bool has = (M != -CUDART_INF_F) && (L > 0.f);
-    const float inv = has ? vscale / L : 0.f;
-    const int t = r / p.G, j = r - t * p.G;
-    const size_t grow = (static_cast<size_t>(b) * p.T + t) * p.num_q_heads + kvh * p.G + j;
-    // natural-log LSE from base-2 running values
-    const float lse_val = has ? (M + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
+    const long long off = s_orow[r] + d;
     if (final_out) {
-      __half2 h01 = __floats2half2_rn(acc.x * inv, acc.y * inv);
-      __half2 h23 = __floats2half2_rn(acc.z * inv, acc.w * inv);
+      __half2 h01 = __floats2half2_rn(acc.x, acc.y);
+      __half2 h23 = __floats2half2_rn(acc.z, acc.w);
       uint2 packed;
       packed.x = *reinterpret_cast<uint32_t*>(&h01);
       packed.y = *reinterpret_cast<uint32_t*>(&h23);
-      *reinterpret_cast<uint2*>(p.out + grow * D + d) = packed;
-      if (d == 0) p.lse[grow] = lse_val;
+      *reinterpret_cast<uint2*>(p.out + off) = packed;
     } else {
-      float* dst = p.o_part + (grow * p.num_splits + split) * D + d;
-      *reinterpret_cast<float4*>(dst) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-      if (d == 0) p.lse_part[grow * p.num_splits + split] = lse_val;
+      *reinterpret_cast<float4*>(p.o_part + off) = acc;
     }
   }
 }
