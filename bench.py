@@ -316,7 +316,7 @@ def run_gpu(args):
         cpu = oracle_sample(args.workload, budget_s=args.cpu_budget)
 
     wid = args.workload
-    spec = workloads.CONFIGS[wid]
+    spec = workloads.ALL[wid]
     case = workloads.make_case(spec, seed=rank_seed(spec, rank))
     dw = DeviceWorkload(case, torch, pf)
     flush = L2Flush(torch)
@@ -383,15 +383,17 @@ def run_gpu(args):
     del dw
     torch.cuda.empty_cache()
     if world == 1 and not args.no_per_config:
-        line["per_config"] = per_config(torch, pf, flush, wid, peak, args)
+        line["per_config"] = per_config(torch, pf, flush, wid, peak, args, workloads.CONFIGS)
+        line["extensions"] = per_config(torch, pf, flush, wid, peak, args, workloads.EXTENSIONS)
+        line["extensions"]["zero_blocks"] = zero_blocks_measure(torch, pf, flush, peak, args)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
-def per_config(torch, pf, flush, skip, peak, args):
+def per_config(torch, pf, flush, skip, peak, args, configs):
     res = {}
-    for cid, spec in workloads.CONFIGS.items():
+    for cid, spec in configs.items():
         if cid == skip or cid in args.skip_configs:
             continue
         case = workloads.make_case(spec)
@@ -410,13 +412,56 @@ def per_config(torch, pf, flush, skip, peak, args):
     return res
 
 
+def zero_blocks_measure(torch, pf, flush, peak, args):
+    """Zeroing of reused blocks: 64 of the 128 blocks of a pool shaped like the 128K decode's
+    (Hkv 4, 2048-token pages, D 256, E4M3), both pools: 256 MiB written per call, timed like a
+    step (L2 flushed before each call). The oracle zeroes 8 blocks of the same shape on the host
+    beside it."""
+    from oracle import append as oappend
+    nb_pool, n, hkv, page, d = 128, 64, 4, 2048, 256
+    k = torch.empty((nb_pool, hkv, page, d), dtype=torch.uint8, device="cuda")
+    v = torch.empty_like(k)
+    ids = torch.from_numpy(np.random.default_rng(7).permutation(nb_pool)[:n].astype(np.int32)).cuda()
+    nbytes = 2 * n * hkv * page * d
+    for _ in range(3):
+        flush()
+        pf.pfkv_kv_cache_zero_blocks(k, v, ids, "e4m3")
+    steps = max(5, min(args.steps, 50))
+    evs = []
+    for _ in range(steps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        pf.pfkv_kv_cache_zero_blocks(k, v, ids, "e4m3")
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+    assert pf.pfkv_device_errors(clear=True) == 0
+    # the oracle beside it, on a host pool of the same block shape
+    hk = np.ones((16, hkv, page, d), np.uint8)
+    hv = np.ones_like(hk)
+    t0 = time.perf_counter()
+    oappend.zero_blocks(hk, hv, np.arange(0, 16, 2, dtype=np.int32))
+    cpu_s = time.perf_counter() - t0
+    cpu_bytes = 2 * 8 * hkv * page * d
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del k, v
+    torch.cuda.empty_cache()
+    return {"workload": "zero 64 reused blocks (Hkv4, page 2048, D256, E4M3), K and V pools: 256 MiB written",
+            "GB/s": round(gbs, 1), "ms_per_call": round(ms, 5), "frac_of_peak": round(gbs / peak, 4),
+            "bound": "hbm (writes)", "steps": steps,
+            "cpu_baseline": {"value": round(cpu_bytes / cpu_s / 1e9, 2), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": "8 blocks of the same shape zeroed on the host"}}
+
+
 # ----------------------------------------------------------------------------- oracle arm
 
 def _oracle_worker_init(wid, seed):
     global _OW
     import numpy as _np  # noqa: F401
     from oracle import append as oappend
-    case = workloads.make_case(workloads.CONFIGS[wid], seed=seed)
+    case = workloads.make_case(workloads.ALL[wid], seed=seed)
     s = case.spec
     dt = np.float16 if s.kv_dtype == "fp16" else np.uint8
     shape = (case.num_blocks, s.num_kv_heads, s.page_size, s.head_dim)
@@ -457,7 +502,11 @@ class OraclePool:
         for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
             os.environ[var] = "1"
         self.cores = len(os.sched_getaffinity(0))
-        self.spec = workloads.CONFIGS[wid]
+        self.spec = workloads.ALL[wid]
+        # every worker builds the whole seeded workload: on the 1 GB workloads a few workers keep
+        # that set-up (and its host memory) bounded
+        if workloads.kv_bytes_of(self.spec) > (256 << 20):
+            self.cores = min(self.cores, 4)
         seed = self.spec.seed if seed is None else seed
         self.pool = mp.get_context("spawn").Pool(self.cores, initializer=_oracle_worker_init, initargs=(wid, seed))
         self.pool.map(abs, range(self.cores))  # wait until every worker holds its inputs
@@ -506,7 +555,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    spec = workloads.CONFIGS[args.workload]
+    spec = workloads.ALL[args.workload]
     vals = []
     info = None
     per = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
@@ -535,7 +584,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(workloads.ALL))
     ap.add_argument("--impl", default="pfkv", choices=["pfkv", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true")

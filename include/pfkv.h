@@ -12,7 +12,8 @@
  *   [R1] "1Cat-vLLM" (README), sections "What is new in 1.0.0" and
  *        "Optional experimental feature: FP8 KV cache";
  *   [R2] "1Cat-vLLM 1.5.0" (release notes), sections "Production DFlash2 on
- *        V100" and "Flash-V100 long-context improvements";
+ *        V100", "Flash-V100 long-context improvements" and "Reliability and
+ *        correctness fixes";
  *   [R3] "SM70 release profile and acceleration status", the profile
  *        paragraph (2048-token KV blocks) and the override table.
  * Each entry point below names the passage that defines its operation.
@@ -69,7 +70,8 @@ typedef enum {
 
 /* Bits of the per-device error word (pfkv_device_errors). */
 #define PFKV_DEVERR_SLOT      0x1u  /* append: slot >= num_blocks * page_size (token skipped) */
-#define PFKV_DEVERR_BLOCK_ID  0x2u  /* decode: block_table entry outside [0, num_blocks) (block 0 read instead) */
+#define PFKV_DEVERR_BLOCK_ID  0x2u  /* decode: block_table entry outside [0, num_blocks) (block 0 read instead);
+                                       zero_blocks: listed id >= num_blocks (skipped) */
 #define PFKV_DEVERR_SEQ_LEN   0x4u  /* decode: seq_len < 0 or > min(max_seq_len, max_blocks_per_seq * page_size) (clamped) */
 #define PFKV_DEVERR_TIMEOUT   0x8u  /* decode: a pipeline wait exceeded its iteration limit (CTA abandoned its work) */
 
@@ -83,6 +85,7 @@ typedef enum {
 #define PFKV_CAP_PAGE_2048      0x200u
 #define PFKV_CAP_PAGE_POW2_ANY  0x400u  /* any power-of-two page size from 16 to 2048 */
 #define PFKV_CAP_Q_TOKENS_1_8   0x1000u /* 1..8 causal query tokens per sequence */
+#define PFKV_CAP_Q_TOKENS_1_16  0x4000u /* 1..16 causal query tokens (a q16 verify), rows <= 64 */
 #define PFKV_CAP_SPLIT_KV       0x2000u /* split-KV partitions + LSE merge kernel */
 
 /*
@@ -116,6 +119,29 @@ PFKV_API pfkv_status pfkv_kv_cache_append(const void* k_new, const void* v_new,
                                  int num_blocks, pfkv_kv_dtype dtype,
                                  const float* k_scale, const float* v_scale,
                                  pfkv_stream_t stream);
+
+/*
+ * pfkv_kv_cache_zero_blocks -- clear every byte of the listed blocks in both
+ * pools (all KV heads, all page offsets), so that a block handed to a new
+ * sequence holds nothing of its previous owner ([R2] "Reliability and
+ * correctness fixes": newly reused KV blocks are zeroed before attention, on
+ * the device, with no host staging). The zero byte is +0 in every cache
+ * dtype.
+ *
+ *   k_cache, v_cache device pools as described above, 16-byte aligned
+ *   block_ids      device, int32 [n_ids]; a negative id is skipped; an id >=
+ *                  num_blocks is skipped and sets PFKV_DEVERR_BLOCK_ID;
+ *                  repeated ids are allowed
+ *   head_dim       up to 1024, with rows of a multiple of 16 bytes (a
+ *                  multiple of 16 for FP8, of 8 for fp16)
+ * n_ids == 0 enqueues nothing and returns PFKV_OK. Blocks not listed are not
+ * written.
+ */
+PFKV_API pfkv_status pfkv_kv_cache_zero_blocks(void* k_cache, void* v_cache,
+                                      const int32_t* block_ids, int n_ids,
+                                      int num_kv_heads, int head_dim, int page_size,
+                                      int num_blocks, pfkv_kv_dtype dtype,
+                                      pfkv_stream_t stream);
 
 /*
  * pfkv_decode_plan -- the split-KV partition pfkv_paged_attention_decode
@@ -183,8 +209,8 @@ PFKV_API size_t pfkv_decode_workspace_bytes(int num_seqs, int num_q_tokens, int 
  *   workspace      device scratch of at least pfkv_decode_workspace_bytes()
  *                  (256-byte aligned; may be NULL when that is 0)
  * Supported: head_dim 128 or 256; page_size a power of two in [16, 2048];
- * 1 <= num_q_tokens <= 8; num_q_heads % num_kv_heads == 0 and
- * num_q_tokens * g <= 64.
+ * 1 <= num_q_tokens <= 16 (e.g. 15 drafts + 1 for a q16 verify);
+ * num_q_heads % num_kv_heads == 0 and num_q_tokens * g <= 64.
  *
  * Arithmetic (within 2e-3 of the exact out and 1e-4 of the exact lse on
  * unit-scale inputs): cache values are decoded exactly; logits are fp32

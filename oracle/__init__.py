@@ -15,7 +15,8 @@ What it computes (plain definitions, numpy float64):
                    mantissa; subnormals; E4M3 has no infinity).
 * ``append``    -- quantise-and-append of new fp16 K/V into a paged cache
                    laid out ``[num_blocks, Hkv, P, D]`` through an int64 slot
-                   mapping (the reshape-and-cache step).
+                   mapping (the reshape-and-cache step). Also the zeroing of
+                   reused blocks.
 * ``attention`` -- paged decode / grouped causal verify attention over that
                    cache: gather by block table, FP8 decode, per-tensor
                    scales, scaled softmax with natural-log LSE.

@@ -90,3 +90,18 @@ def append_bulk(cache: np.ndarray, new: np.ndarray, slot_mapping: np.ndarray,
         vals = quantise(vals, scale, kv_dtype)
     # cache[block, :, off, :] with fancy indices on axes 0 and 2
     cache[block, :, off, :] = vals
+
+
+def zero_blocks(k_cache: np.ndarray, v_cache: np.ndarray, block_ids) -> None:
+    """Clear the listed blocks of both pools in place ("1Cat-vLLM 1.5.0", section "Reliability
+    and correctness fixes": newly reused KV blocks are zeroed before attention).
+
+    Pools are ``[num_blocks, Hkv, P, D]``; every element of a listed block becomes the zero
+    byte pattern (+0 in fp16, E4M3 and E5M2 alike). A negative id means "no block" and is
+    skipped, as is an id past the pool (the device path reports that one).
+    """
+    nb = k_cache.shape[0]
+    for bid in np.asarray(block_ids, dtype=np.int64).ravel():
+        if 0 <= bid < nb:
+            k_cache[bid] = 0
+            v_cache[bid] = 0

@@ -36,6 +36,7 @@ PFKV_DEVERR_TIMEOUT = 0x8
 # every entry point declared in include/pfkv.h
 EXPORTS = [
     "pfkv_kv_cache_append",
+    "pfkv_kv_cache_zero_blocks",
     "pfkv_decode_plan",
     "pfkv_decode_workspace_bytes",
     "pfkv_paged_attention_decode",
@@ -74,6 +75,8 @@ def load(path: str | None = None):
     vp, i32, i64p, f32p, u32p = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)
     lib.pfkv_kv_cache_append.argtypes = [vp, vp, vp, vp, i64p, i32, i32, i32, i32, i32, i32, f32p, f32p, vp]
     lib.pfkv_kv_cache_append.restype = i32
+    lib.pfkv_kv_cache_zero_blocks.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
+    lib.pfkv_kv_cache_zero_blocks.restype = i32
     lib.pfkv_decode_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                      ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
     lib.pfkv_decode_plan.restype = i32
@@ -117,6 +120,14 @@ def _stream(stream):
 
 def _kv(dtype) -> int:
     return KV_DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+
+
+def pfkv_kv_cache_zero_blocks(k_cache, v_cache, block_ids, kv_dtype, stream=None):
+    """Zero the listed blocks of both pools [num_blocks, Hkv, P, D]; block_ids int32 [n] (negative = skip)."""
+    lib = load()
+    nb, hkv, page, d = k_cache.shape
+    _check(lib.pfkv_kv_cache_zero_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_ids), block_ids.numel(), hkv, d,
+                                         page, nb, _kv(kv_dtype), _stream(stream)))
 
 
 def pfkv_kv_cache_append(k_new, v_new, k_cache, v_cache, slot_mapping, page_size, kv_dtype,

@@ -203,7 +203,7 @@ pfkv_status check_shape(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv
                 num_seqs, Hq, Hkv, max_seq_len, num_splits);
   if (Hq % Hkv != 0) return fail(PFKV_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d", Hq, Hkv);
   if (!valid_dtype(dtype)) return fail(PFKV_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(dtype));
-  if (T < 1 || T > 8) return fail(PFKV_ERR_UNSUPPORTED, "num_q_tokens %d outside 1..8", T);
+  if (T < 1 || T > 16) return fail(PFKV_ERR_UNSUPPORTED, "num_q_tokens %d outside 1..16", T);
   if (D != 128 && D != 256) return fail(PFKV_ERR_UNSUPPORTED, "head_dim %d (supported: 128, 256)", D);
   if (!is_pow2(P) || P < 16 || P > 2048)
     return fail(PFKV_ERR_UNSUPPORTED, "page_size %d (supported: powers of two 16..2048)", P);
@@ -294,7 +294,7 @@ const char* pfkv_last_error(void) { return g_last_error.c_str(); }
 uint32_t pfkv_capabilities(void) {
   return PFKV_CAP_KV_FP16 | PFKV_CAP_KV_FP8_E4M3 | PFKV_CAP_KV_FP8_E5M2 | PFKV_CAP_HEAD_DIM_128 |
          PFKV_CAP_HEAD_DIM_256 | PFKV_CAP_PAGE_16 | PFKV_CAP_PAGE_2048 | PFKV_CAP_PAGE_POW2_ANY |
-         PFKV_CAP_Q_TOKENS_1_8 | PFKV_CAP_SPLIT_KV;
+         PFKV_CAP_Q_TOKENS_1_8 | PFKV_CAP_Q_TOKENS_1_16 | PFKV_CAP_SPLIT_KV;
 }
 
 pfkv_status pfkv_device_errors(uint32_t* flags, int clear) {
@@ -338,6 +338,34 @@ pfkv_status pfkv_kv_cache_append(const void* k_new, const void* v_new, void* k_c
                     slot_mapping, n_tok, num_kv_heads, head_dim, page_size, num_blocks, kv_of(dtype), k_scale, v_scale,
                     err, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PFKV_OK : cuda_fail(e, "append launch");
+}
+
+pfkv_status pfkv_kv_cache_zero_blocks(void* k_cache, void* v_cache, const int32_t* block_ids, int n_ids,
+                                      int num_kv_heads, int head_dim, int page_size, int num_blocks,
+                                      pfkv_kv_dtype dtype, pfkv_stream_t stream) {
+  if (n_ids < 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0 || num_blocks <= 0)
+    return fail(PFKV_ERR_INVALID_ARG, "bad size (n_ids=%d Hkv=%d D=%d P=%d num_blocks=%d)", n_ids, num_kv_heads,
+                head_dim, page_size, num_blocks);
+  if (!valid_dtype(dtype)) return fail(PFKV_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(dtype));
+  // every cache row a whole number of 16-byte stores
+  const int row_bytes = head_dim * (dtype == PFKV_KV_FP16 ? 2 : 1);
+  if (row_bytes % 16 != 0 || head_dim > 1024)
+    return fail(PFKV_ERR_UNSUPPORTED, "head_dim %d (rows of a multiple of 16 bytes, at most 1024 elements)",
+                head_dim);
+  if (n_ids == 0) return PFKV_OK;
+  if (!k_cache || !v_cache || !block_ids) return fail(PFKV_ERR_INVALID_ARG, "null pointer");
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15)
+    return fail(PFKV_ERR_INVALID_ARG, "cache pointers must be 16-byte aligned");
+  const long long elt = dtype == PFKV_KV_FP16 ? 2 : 1;
+  const long long block_bytes = static_cast<long long>(num_kv_heads) * page_size * head_dim * elt;
+  int dev;
+  unsigned* err;
+  cudaError_t e = current_device(&dev);
+  if (e == cudaSuccess) e = err_word(dev, &err);
+  if (e != cudaSuccess) return cuda_fail(e, "device set-up");
+  e = launch_zero_blocks(k_cache, v_cache, block_ids, n_ids, block_bytes, num_blocks, err,
+                         reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PFKV_OK : cuda_fail(e, "zero_blocks launch");
 }
 
 pfkv_status pfkv_decode_plan(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads, int head_dim,

@@ -98,6 +98,10 @@ cudaError_t launch_lse_merge(__half* out, float* lse, const float* o_parts, cons
                              int num_parts, int head_dim, const int32_t* seq_lens, int rows_per_seq,
                              int split_tokens, int max_seq_len, int max_len_cap, cudaStream_t stream);
 
+// zero_blocks.cu
+cudaError_t launch_zero_blocks(void* k_cache, void* v_cache, const int32_t* block_ids, int n_ids, long long block_bytes,
+                               int num_blocks, unsigned* err, cudaStream_t stream);
+
 // append.cu
 cudaError_t launch_append(const __half* k_new, const __half* v_new, void* k_cache, void* v_cache,
                           const int64_t* slots, int n_tok, int num_kv_heads, int head_dim, int page_size,

@@ -80,6 +80,17 @@ CONFIGS = {
                 pool_factor=1.25, append_new=1, seed=1005),
 }
 
+# Workloads of rows built beyond the five, measured with the same harness and reported apart:
+# a q16 verify (15 drafts + 1) at 256K keys, the q8 verifier's shape class with 16 query tokens
+# per sequence and 4 query heads per KV head (64 rows per KV head).
+EXTENSIONS = {
+    6: CaseSpec("q16 speculative verify: 2 seqs x 262144, q16 causal, Hq16/Hkv4, D256, E5M2 KV, page 2048",
+                contexts=(262144,) * 2, num_q_tokens=16, num_q_heads=16, num_kv_heads=4,
+                head_dim=256, page_size=2048, kv_dtype="e5m2", seed=1006),
+}
+
+ALL = {**CONFIGS, **EXTENSIONS}
+
 
 @dataclass
 class Case:
@@ -112,6 +123,14 @@ class Case:
         """K+V cache bytes one decode pass reads (every key of every unit once)."""
         elt = 2 if self.spec.kv_dtype == "fp16" else 1
         return int(self.seq_lens.astype(np.int64).sum()) * self.spec.num_kv_heads * self.spec.head_dim * elt * 2
+
+
+def kv_bytes_of(spec: CaseSpec) -> int:
+    """Approximate K+V cache bytes of a workload (a log-uniform batch counted at its upper bound)."""
+    c = spec.contexts
+    total = c[2] * c[3] if len(c) and c[0] == "loguniform" else int(sum(c))
+    elt = 2 if spec.kv_dtype == "fp16" else 1
+    return int(total) * spec.num_kv_heads * spec.head_dim * elt * 2
 
 
 def _contexts(spec: CaseSpec, rng) -> np.ndarray:
@@ -189,7 +208,7 @@ def make_case(spec: CaseSpec, seed: int | None = None) -> Case:
 
 def small_spec(cfg_id: int, **over) -> CaseSpec:
     """A reduced copy of a benchmark workload (same dtype/heads/page layout)."""
-    return replace(CONFIGS[cfg_id], **over)
+    return replace(ALL[cfg_id], **over)
 
 
 def split_fill(case: Case, units: list[tuple[int, int]] | None = None):

@@ -46,17 +46,19 @@ def test_status_strings_and_capabilities(pflib):
                      (3, "PFKV_ERR_WORKSPACE"), (4, "PFKV_ERR_CUDA"), (5, "PFKV_ERR_DEVICE_CHECK")]:
         assert pf.pfkv_status_string(st) == name
     caps = pf.pfkv_capabilities()
-    for bit in (0x1, 0x2, 0x4, 0x10, 0x20, 0x100, 0x200, 0x1000, 0x2000):
+    for bit in (0x1, 0x2, 0x4, 0x10, 0x20, 0x100, 0x200, 0x1000, 0x2000, 0x4000):
         assert caps & bit
 
 
 @pytest.mark.parametrize("args,status", [
-    (dict(T=9), pf.PFKV_ERR_UNSUPPORTED),
+    (dict(T=17), pf.PFKV_ERR_UNSUPPORTED),
+    (dict(T=0), pf.PFKV_ERR_UNSUPPORTED),
     (dict(D=64), pf.PFKV_ERR_UNSUPPORTED),
     (dict(P=24), pf.PFKV_ERR_UNSUPPORTED),
     (dict(P=4096), pf.PFKV_ERR_UNSUPPORTED),
     (dict(Hq=30), pf.PFKV_ERR_INVALID_ARG),
     (dict(T=8, Hq=72, Hkv=8), pf.PFKV_ERR_UNSUPPORTED),  # 8 tokens x group 9 = 72 rows > 64
+    (dict(T=16, Hq=40, Hkv=8), pf.PFKV_ERR_UNSUPPORTED),  # 16 tokens x group 5 = 80 rows > 64
     (dict(B=-1), pf.PFKV_ERR_INVALID_ARG),
     (dict(kv=7), pf.PFKV_ERR_INVALID_ARG),
 ])
@@ -66,6 +68,13 @@ def test_plan_rejects_bad_shapes(pflib, args, status):
     with pytest.raises(pf.PfkvError) as ei:
         pf.pfkv_decode_plan(a["B"], a["T"], a["Hq"], a["Hkv"], a["D"], a["P"], a["kv"], a["msl"], a["S"])
     assert ei.value.status == status
+
+
+@pytest.mark.parametrize("T,Hq,Hkv", [(9, 16, 4), (16, 16, 4), (16, 8, 8), (12, 40, 8)])
+def test_plan_accepts_q16_verify_shapes(pflib, T, Hq, Hkv):
+    # up to 16 query tokens per sequence while the rows per KV head (T * g) stay within 64
+    S, C = pf.pfkv_decode_plan(2, T, Hq, Hkv, 256, 2048, "e5m2", 262144, 19)
+    assert S == 19 and S * C >= 262144
 
 
 @pytest.mark.parametrize("msl,req,exp", [
@@ -110,3 +119,23 @@ def test_fragment_layout_checker(tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
     assert "layout ok" in r.stdout
+
+
+def test_zero_blocks_validation_before_any_launch(pflib):
+    lib = pf.load()
+    # no ids: a no-op; bad head_dim: unsupported; null pointers / misaligned pools: invalid
+    assert lib.pfkv_kv_cache_zero_blocks(None, None, None, 0, 8, 128, 16, 10, 1, None) == pf.PFKV_OK
+    assert lib.pfkv_kv_cache_zero_blocks(None, None, None, 4, 8, 100, 16, 10, 1, None) == pf.PFKV_ERR_UNSUPPORTED
+    assert lib.pfkv_kv_cache_zero_blocks(None, None, None, 4, 8, 128, 16, 10, 1, None) == pf.PFKV_ERR_INVALID_ARG
+    assert lib.pfkv_kv_cache_zero_blocks(None, None, None, -1, 8, 128, 16, 10, 1, None) == pf.PFKV_ERR_INVALID_ARG
+    assert lib.pfkv_kv_cache_zero_blocks(ctypes.c_void_p(16), ctypes.c_void_p(24), ctypes.c_void_p(32), 4, 8, 128,
+                                         16, 10, 1, None) == pf.PFKV_ERR_INVALID_ARG
+    assert "aligned" in pf.pfkv_last_error()
+    assert lib.pfkv_kv_cache_zero_blocks(None, None, None, 4, 8, 128, 16, 10, 9, None) == pf.PFKV_ERR_INVALID_ARG
+
+
+def test_zero_blocks_rejects_rows_of_partial_16_byte_stores(pflib):
+    lib = pf.load()
+    # FP8 rows of 8 bytes (head_dim 8) would need an 8-byte tail store: unsupported; fp16 rows of 16 bytes are fine
+    assert lib.pfkv_kv_cache_zero_blocks(None, None, None, 4, 1, 8, 1, 10, 1, None) == pf.PFKV_ERR_UNSUPPORTED
+    assert lib.pfkv_kv_cache_zero_blocks(None, None, None, 4, 1, 8, 1, 10, 0, None) == pf.PFKV_ERR_INVALID_ARG

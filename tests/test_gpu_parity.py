@@ -24,6 +24,7 @@ SMALL = {
     "c3-long-e4m3-small": workloads.small_spec(3, contexts=(5000,)),
     "c4-verify-q8-e5m2-small": workloads.small_spec(4, contexts=(4100, 2500)),
     "c5-mixed-e4m3-small": workloads.small_spec(5, contexts=("loguniform", 30, 700, 64)),
+    "x6-verify-q16-e5m2-small": workloads.small_spec(6, contexts=(4100, 2500)),
 }
 
 _cache = {}

@@ -77,3 +77,35 @@ def test_append_bulk_equals_token_loop(cfg):
     append.append(a, case.k_fill, case.slot_fill, spec.page_size, case.k_scale, spec.kv_dtype)
     append.append_bulk(b, case.k_fill, case.slot_fill, spec.page_size, case.k_scale, spec.kv_dtype)
     assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+@pytest.mark.parametrize("kv", ["fp16", "e4m3", "e5m2"])
+def test_zero_blocks_clears_listed_blocks_only(kv):
+    # the reused-block zeroing: listed blocks become all-zero bytes, which decode to +0 in every
+    # cache format; every other block keeps its bytes; negative and out-of-pool ids are skipped
+    from oracle import append as oappend, fp8
+    rng = np.random.default_rng(5)
+    shape = (9, 2, 4, 8)
+    if kv == "fp16":
+        kc0 = rng.integers(0, 1 << 16, size=shape, dtype=np.uint16).view(np.float16)
+        vc0 = rng.integers(0, 1 << 16, size=shape, dtype=np.uint16).view(np.float16)
+    else:
+        kc0 = rng.integers(0, 256, size=shape, dtype=np.uint8)
+        vc0 = rng.integers(0, 256, size=shape, dtype=np.uint8)
+    kc, vc = kc0.copy(), vc0.copy()
+    ids = [3, -1, 7, 3, 9, 120, 0]
+    oappend.zero_blocks(kc, vc, ids)
+    listed = {0, 3, 7}
+    for b in range(shape[0]):
+        if b in listed:
+            assert not kc[b].view(np.uint8).any() and not vc[b].view(np.uint8).any()
+        else:
+            assert np.array_equal(kc[b].view(np.uint8), kc0[b].view(np.uint8))
+            assert np.array_equal(vc[b].view(np.uint8), vc0[b].view(np.uint8))
+    if kv == "fp16":
+        z = np.zeros(1, np.uint16).view(np.float16)[0]
+        assert z == 0 and not np.signbit(z)
+    else:
+        fmt = fp8.E4M3 if kv == "e4m3" else fp8.E5M2
+        z = fp8.decode(np.zeros(1, np.uint8), fmt)[0]
+        assert z == 0 and not np.signbit(z)

@@ -87,6 +87,7 @@ BRUTE_CASES = [
     dict(kv="e5m2", T=3, g=2, D=8, P=16, contexts=(19, 3)),
     dict(kv="e4m3", T=3, g=1, D=4, P=16, contexts=(33,), Hkv=3),
     dict(kv="e5m2", T=1, g=2, D=8, P=4, contexts=(40, 17), v_dist="uniform", k_outlier_frac=0.1),
+    dict(kv="e4m3", T=16, g=2, D=4, P=4, contexts=(21, 16)),  # q16 verify: 15 drafts + 1
 ]
 
 
@@ -163,17 +164,17 @@ def pin_single_key(att):
 
 
 def pin_causal_rows_are_shorter_decodes(att):
-    case = workloads.make_case(tiny_spec("e5m2", T=3, g=2, P=4, contexts=(22, 11)))
-    kc, vc = oracle_caches(case)
-    o, l = run(att, case, kc, vc)
-    T = 3
-    for t in range(T):
-        q1 = case.q.reshape(case.B, T, *case.q.shape[1:])[:, t]
-        sl = case.seq_lens - (T - 1 - t)
-        o1, l1 = run(att, case, kc, vc, q=q1, num_q_tokens=1, seq_lens=sl)
-        if not (np.allclose(o1, o.reshape(case.B, T, *o.shape[1:])[:, t], rtol=0, atol=1e-14)
-                and np.allclose(l1, l.reshape(case.B, T, -1)[:, t], rtol=0, atol=1e-14)):
-            return False
+    for T, contexts in ((3, (22, 11)), (16, (30, 17))):
+        case = workloads.make_case(tiny_spec("e5m2", T=T, g=2, P=4, contexts=contexts))
+        kc, vc = oracle_caches(case)
+        o, l = run(att, case, kc, vc)
+        for t in range(T):
+            q1 = case.q.reshape(case.B, T, *case.q.shape[1:])[:, t]
+            sl = case.seq_lens - (T - 1 - t)
+            o1, l1 = run(att, case, kc, vc, q=q1, num_q_tokens=1, seq_lens=sl)
+            if not (np.allclose(o1, o.reshape(case.B, T, *o.shape[1:])[:, t], rtol=0, atol=1e-14)
+                    and np.allclose(l1, l.reshape(case.B, T, -1)[:, t], rtol=0, atol=1e-14)):
+                return False
     return True
 
 
