@@ -200,8 +200,9 @@ class DeviceWorkload:
         shape = (case.num_blocks, s.num_kv_heads, s.page_size, s.head_dim)
         self.k_cache = torch.zeros(shape, dtype=elt, device=dev)
         self.v_cache = torch.zeros(shape, dtype=elt, device=dev)
-        self.k_scale = torch.tensor([float(case.k_scale)], dtype=torch.float32, device=dev)
-        self.v_scale = torch.tensor([float(case.v_scale)], dtype=torch.float32, device=dev)
+        # one float per pool, or one per KV head (the binding then sets PFKV_KV_SCALES_PER_HEAD)
+        self.k_scale = torch.tensor(np.asarray(case.k_scale, np.float32).reshape(-1), device=dev)
+        self.v_scale = torch.tensor(np.asarray(case.v_scale, np.float32).reshape(-1), device=dev)
         n = case.k_fill.shape[0]
         step = max(1, (1 << 24) // (s.num_kv_heads * s.head_dim))
         for a in range(0, n, step):
@@ -486,8 +487,10 @@ def _oracle_unit(u):
                 kc[blk, kvh, off] = case.k_new[i, kvh]
                 vc[blk, kvh, off] = case.v_new[i, kvh]
             else:
-                kc[blk, kvh, off] = oappend.quantise(case.k_new[i, kvh], case.k_scale, s.kv_dtype)
-                vc[blk, kvh, off] = oappend.quantise(case.v_new[i, kvh], case.v_scale, s.kv_dtype)
+                ks = np.asarray(case.k_scale, np.float32).reshape(-1)
+                vs = np.asarray(case.v_scale, np.float32).reshape(-1)
+                kc[blk, kvh, off] = oappend.quantise(case.k_new[i, kvh], ks[kvh % ks.size], s.kv_dtype)
+                vc[blk, kvh, off] = oappend.quantise(case.v_new[i, kvh], vs[kvh % vs.size], s.kv_dtype)
     oatt.paged_attention(case.q, kc, vc, case.block_table, case.seq_lens, s.num_q_tokens, s.num_kv_heads,
                          s.page_size, s.kv_dtype, case.k_scale, case.v_scale, case.softmax_scale, units=[u])
     elt = 2 if s.kv_dtype == "fp16" else 1

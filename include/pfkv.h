@@ -68,6 +68,18 @@ typedef enum {
   PFKV_KV_FP8_E5M2 = 2   /* E5M2: bias 15, max 57344, IEEE-style inf/NaN */
 } pfkv_kv_dtype;
 
+/*
+ * OR this flag into the dtype argument of pfkv_kv_cache_append,
+ * pfkv_paged_attention_decode or pfkv_paged_attention_decode_static_scratch
+ * with an FP8 cache to pass one static scale per KV head: k_scale and v_scale
+ * then point to num_kv_heads floats each, and KV head h is quantised,
+ * decoded and scaled with k_scale[h] / v_scale[h]. (The pages use one
+ * per-tensor scale per pool; per-head scales are the generalisation of it.)
+ * pfkv_decode_plan, pfkv_decode_workspace_bytes and pfkv_kv_cache_zero_blocks
+ * accept and ignore the flag; with an fp16 cache it is an invalid argument.
+ */
+#define PFKV_KV_SCALES_PER_HEAD 0x100
+
 /* Bits of the per-device error word (pfkv_device_errors). */
 #define PFKV_DEVERR_SLOT      0x1u  /* append: slot >= num_blocks * page_size (token skipped) */
 #define PFKV_DEVERR_BLOCK_ID  0x2u  /* decode: block_table entry outside [0, num_blocks) (block 0 read instead);
@@ -87,6 +99,7 @@ typedef enum {
 #define PFKV_CAP_Q_TOKENS_1_8   0x1000u /* 1..8 causal query tokens per sequence */
 #define PFKV_CAP_Q_TOKENS_1_16  0x4000u /* 1..16 causal query tokens (a q16 verify), rows <= 64 */
 #define PFKV_CAP_SPLIT_KV       0x2000u /* split-KV partitions + LSE merge kernel */
+#define PFKV_CAP_SCALES_PER_HEAD 0x8000u /* PFKV_KV_SCALES_PER_HEAD: one FP8 scale per KV head */
 
 /*
  * pfkv_kv_cache_append -- quantise new K/V tokens and write them into their
@@ -108,7 +121,8 @@ typedef enum {
  *   k_new, v_new   device, fp16 [n_tok][num_kv_heads][head_dim], 16-byte aligned
  *   k_cache, v_cache device pools as described above, 16-byte aligned
  *   slot_mapping   device, int64 [n_tok]
- *   k_scale, v_scale device, one float each; ignored (may be NULL) for FP16
+ *   k_scale, v_scale device, one float each (num_kv_heads each with
+ *                  PFKV_KV_SCALES_PER_HEAD); ignored (may be NULL) for FP16
  *   head_dim       a multiple of 8 (any value up to 1024)
  * n_tok == 0 enqueues nothing and returns PFKV_OK.
  */
@@ -203,7 +217,8 @@ PFKV_API size_t pfkv_decode_workspace_bytes(int num_seqs, int num_q_tokens, int 
  *   block_table    device, int32 [num_seqs][max_blocks_per_seq]; entries past
  *                  a sequence's last page are never read
  *   seq_lens       device, int32 [num_seqs]
- *   k_scale, v_scale device floats; ignored (may be NULL) for FP16 caches
+ *   k_scale, v_scale device floats, one each (num_kv_heads each with
+ *                  PFKV_KV_SCALES_PER_HEAD); ignored (may be NULL) for FP16 caches
  *   max_seq_len    host upper bound on seq_lens (sizes the split plan)
  *   num_splits     see pfkv_decode_plan (0 = automatic)
  *   workspace      device scratch of at least pfkv_decode_workspace_bytes()

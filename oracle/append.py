@@ -34,17 +34,32 @@ import numpy as np
 from . import fp8
 
 
-def quantise(x16: np.ndarray, scale: float, fmt) -> np.ndarray:
-    """uint8 codes of fp16 values divided by a float32 per-tensor scale."""
+def quantise(x16: np.ndarray, scale, fmt) -> np.ndarray:
+    """uint8 codes of fp16 values divided by a float32 scale (a scalar, or an array that
+    broadcasts against ``x16``, e.g. ``[Hkv, 1]`` for one scale per KV head)."""
     x32 = np.asarray(x16, dtype=np.float16).astype(np.float32)
-    s32 = np.float32(scale)
-    q = (x32.astype(np.float64) / np.float64(s32)).astype(np.float32)
+    s32 = np.asarray(scale, dtype=np.float32)
+    q = (x32.astype(np.float64) / s32.astype(np.float64)).astype(np.float32)
     return fp8.encode(q, fmt)
+
+
+def head_scales(scale, num_kv_heads: int):
+    """A per-tensor scale as a float32 scalar, or one scale per KV head (an array of
+    ``num_kv_heads``, the per-head generalisation of the pages' per-tensor static scales) as a
+    float32 ``[Hkv, 1]`` column that broadcasts over ``[..., Hkv, D]``."""
+    s = np.asarray(scale, dtype=np.float32)
+    if s.size == 1:
+        return np.float32(s.reshape(()))
+    if s.size != num_kv_heads:
+        raise ValueError(f"{s.size} scales for {num_kv_heads} KV heads")
+    return s.reshape(num_kv_heads, 1)
 
 
 def append(cache: np.ndarray, new: np.ndarray, slot_mapping: np.ndarray,
            page_size: int, scale, kv_dtype: str) -> None:
     """Write ``new[i]`` (fp16 ``[Hkv, D]``) into ``cache`` at ``slot_mapping[i]``.
+
+    ``scale`` is one float32 for the pool or one per KV head (``[Hkv]``).
 
     ``cache`` is ``uint8 [num_blocks, Hkv, P, D]`` for ``kv_dtype`` in
     ``{"e4m3", "e5m2"}`` or ``float16 [num_blocks, Hkv, P, D]`` for ``"fp16"``.
@@ -55,6 +70,7 @@ def append(cache: np.ndarray, new: np.ndarray, slot_mapping: np.ndarray,
     new = np.asarray(new, dtype=np.float16)
     n_tok = new.shape[0]
     num_blocks = cache.shape[0]
+    scale = head_scales(scale, cache.shape[1])
     for i in range(n_tok):
         slot = int(slot_mapping[i])
         if slot < 0:
@@ -87,7 +103,7 @@ def append_bulk(cache: np.ndarray, new: np.ndarray, slot_mapping: np.ndarray,
     off = slots % page_size
     vals = new[keep]
     if kv_dtype != "fp16":
-        vals = quantise(vals, scale, kv_dtype)
+        vals = quantise(vals, head_scales(scale, cache.shape[1]), kv_dtype)
     # cache[block, :, off, :] with fancy indices on axes 0 and 2
     cache[block, :, off, :] = vals
 

@@ -19,7 +19,10 @@ for sequence b, query token t < T and query head h:
   counts the T query tokens, whose K/V are in the cache) and sees keys
   ``j = 0 .. N_b - T + t`` (causal over its own drafts);
 * key j lives at ``page = block_table[b][j // P]``, ``offset = j % P``;
-* ``k_j = decode(K[page, kvh, offset]) * k_scale`` and likewise ``v_j``;
+* ``k_j = decode(K[page, kvh, offset]) * k_scale`` and likewise ``v_j``
+  (``k_scale`` is the pool's static scale, or KV head kvh's when one scale
+  per KV head is given: the per-head generalisation of the per-tensor
+  scales, a reading of ours -- the pages use per-tensor scales only);
 * ``s_j = softmax_scale * sum_d q_d k_jd``, ``m = max_j s_j``,
   ``w_j = exp(s_j - m)``, ``L = sum_j w_j``;
 * ``out = sum_j w_j v_j / L`` and ``lse = m + ln L`` (natural log, the logits
@@ -72,12 +75,18 @@ def paged_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
     g = Hq // num_kv_heads
     out = np.full((BT, Hq, D), np.nan)
     lse = np.full((BT, Hq), np.nan)
-    ks = np.float64(np.float32(k_scale))
-    vs = np.float64(np.float32(v_scale))
+    # one float32 scale per pool, or one per KV head (an array of num_kv_heads)
+    ks_all = np.asarray(k_scale, dtype=np.float32).astype(np.float64).reshape(-1)
+    vs_all = np.asarray(v_scale, dtype=np.float32).astype(np.float64).reshape(-1)
+    for a in (ks_all, vs_all):
+        if a.size not in (1, num_kv_heads):
+            raise ValueError(f"{a.size} scales for {num_kv_heads} KV heads")
     sm = np.float64(np.float32(softmax_scale))
     if units is None:
         units = [(b, kvh) for b in range(B) for kvh in range(num_kv_heads)]
     for b, kvh in units:
+        ks = ks_all[kvh if ks_all.size > 1 else 0]
+        vs = vs_all[kvh if vs_all.size > 1 else 0]
         n = int(seq_lens[b])
         heads = list(range(kvh * g, (kvh + 1) * g))
         # rows of this unit: (t, head) -> q vector

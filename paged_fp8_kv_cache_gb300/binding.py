@@ -32,6 +32,7 @@ PFKV_DEVERR_SLOT = 0x1
 PFKV_DEVERR_BLOCK_ID = 0x2
 PFKV_DEVERR_SEQ_LEN = 0x4
 PFKV_DEVERR_TIMEOUT = 0x8
+PFKV_KV_SCALES_PER_HEAD = 0x100  # OR into an FP8 dtype: one scale per KV head
 
 # every entry point declared in include/pfkv.h
 EXPORTS = [
@@ -122,6 +123,14 @@ def _kv(dtype) -> int:
     return KV_DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
 
 
+def _kv_scaled(dtype, k_scale) -> int:
+    """The dtype argument, with PFKV_KV_SCALES_PER_HEAD when the scale tensors hold one float per KV head."""
+    kv = _kv(dtype)
+    if k_scale is not None and k_scale.numel() > 1:
+        kv |= PFKV_KV_SCALES_PER_HEAD
+    return kv
+
+
 def pfkv_kv_cache_zero_blocks(k_cache, v_cache, block_ids, kv_dtype, stream=None):
     """Zero the listed blocks of both pools [num_blocks, Hkv, P, D]; block_ids int32 [n] (negative = skip)."""
     lib = load()
@@ -136,7 +145,7 @@ def pfkv_kv_cache_append(k_new, v_new, k_cache, v_cache, slot_mapping, page_size
     lib = load()
     n_tok, hkv, d = k_new.shape
     _check(lib.pfkv_kv_cache_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
-                                    n_tok, hkv, d, page_size, k_cache.shape[0], _kv(kv_dtype),
+                                    n_tok, hkv, d, page_size, k_cache.shape[0], _kv_scaled(kv_dtype, k_scale),
                                     _ptr(k_scale), _ptr(v_scale), _stream(stream)))
 
 
@@ -166,8 +175,9 @@ def pfkv_paged_attention_decode(out, lse, q, k_cache, v_cache, block_table, seq_
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.pfkv_paged_attention_decode(
         _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
-        _ptr(seq_lens), num_seqs, num_q_tokens, hq, num_kv_heads, d, page_size, k_cache.shape[0], _kv(kv_dtype),
-        _ptr(k_scale), _ptr(v_scale), float(softmax_scale), max_seq_len, num_splits, _ptr(workspace), ws_bytes,
+        _ptr(seq_lens), num_seqs, num_q_tokens, hq, num_kv_heads, d, page_size, k_cache.shape[0],
+        _kv_scaled(kv_dtype, k_scale), _ptr(k_scale), _ptr(v_scale), float(softmax_scale), max_seq_len, num_splits,
+        _ptr(workspace), ws_bytes,
         _stream(stream)))
 
 
@@ -180,8 +190,9 @@ def pfkv_paged_attention_decode_static_scratch(out, lse, q, k_cache, v_cache, bl
     hq, d = q.shape[1], q.shape[2]
     _check(lib.pfkv_paged_attention_decode_static_scratch(
         _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
-        _ptr(seq_lens), num_seqs, num_q_tokens, hq, num_kv_heads, d, page_size, k_cache.shape[0], _kv(kv_dtype),
-        _ptr(k_scale), _ptr(v_scale), float(softmax_scale), max_seq_len, num_splits, _stream(stream)))
+        _ptr(seq_lens), num_seqs, num_q_tokens, hq, num_kv_heads, d, page_size, k_cache.shape[0],
+        _kv_scaled(kv_dtype, k_scale), _ptr(k_scale), _ptr(v_scale), float(softmax_scale), max_seq_len, num_splits,
+        _stream(stream)))
 
 
 def pfkv_lse_merge(out, lse, o_parts, lse_parts, stream=None):

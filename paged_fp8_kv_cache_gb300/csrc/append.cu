@@ -1,8 +1,8 @@
 // kv_cache_append: quantise new fp16 K/V tokens with a static per-tensor
-// scale and write them into their cache pages (the KV write path of the
-// fork, "1Cat-vLLM": FP8 KV cache with static scales, no online scale
-// computation; pages of 16 or 2048 tokens, "SM70 release profile and
-// acceleration status").
+// scale (or one per KV head) and write them into their cache pages (the KV
+// write path of the fork, "1Cat-vLLM": FP8 KV cache with static scales, no
+// online scale computation; pages of 16 or 2048 tokens, "SM70 release
+// profile and acceleration status").
 //
 // One thread moves 8 consecutive head-dim elements of one (token, KV head)
 // for both K and V: two 16-byte loads of fp16, two 8-byte stores of FP8
@@ -43,7 +43,8 @@ __global__ void __launch_bounds__(256) append_kernel(const __half* __restrict__ 
                                                      const int64_t* __restrict__ slots, int n_tok, int num_kv_heads,
                                                      int head_dim, int page_size, int num_blocks,
                                                      const float* __restrict__ k_scale,
-                                                     const float* __restrict__ v_scale, unsigned* err) {
+                                                     const float* __restrict__ v_scale, int scale_stride,
+                                                     unsigned* err) {
   const int chunks = head_dim / 8;
   const int64_t per_tok = static_cast<int64_t>(num_kv_heads) * chunks;
   const int64_t total = per_tok * n_tok;
@@ -66,6 +67,10 @@ __global__ void __launch_bounds__(256) append_kernel(const __half* __restrict__ 
       continue;
     }
     const int64_t blk = slot / page_size, off = slot - blk * page_size;
+    if (KV != kKvFp16 && scale_stride != 0) {  // one scale per KV head
+      ks = k_scale[h];
+      vs = v_scale[h];
+    }
     const int64_t src = (tok * num_kv_heads + h) * head_dim + ch * 8;
     const int64_t dst = ((blk * num_kv_heads + h) * page_size + off) * head_dim + ch * 8;
     const uint4 kv = *reinterpret_cast<const uint4*>(k_new + src);
@@ -82,7 +87,8 @@ __global__ void __launch_bounds__(256) append_kernel(const __half* __restrict__ 
 
 cudaError_t launch_append(const __half* k_new, const __half* v_new, void* k_cache, void* v_cache, const int64_t* slots,
                           int n_tok, int num_kv_heads, int head_dim, int page_size, int num_blocks, int kv,
-                          const float* k_scale, const float* v_scale, unsigned* err, cudaStream_t stream) {
+                          const float* k_scale, const float* v_scale, int scale_stride, unsigned* err,
+                          cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(n_tok) * num_kv_heads * (head_dim / 8);
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
@@ -93,15 +99,15 @@ cudaError_t launch_append(const __half* k_new, const __half* v_new, void* k_cach
   switch (kv) {
     case kKvFp16:
       append_kernel<kKvFp16><<<static_cast<int>(blocks), threads, 0, stream>>>(
-          k_new, v_new, kc, vc, slots, n_tok, num_kv_heads, head_dim, page_size, num_blocks, k_scale, v_scale, err);
+          k_new, v_new, kc, vc, slots, n_tok, num_kv_heads, head_dim, page_size, num_blocks, k_scale, v_scale, scale_stride, err);
       break;
     case kKvE4m3:
       append_kernel<kKvE4m3><<<static_cast<int>(blocks), threads, 0, stream>>>(
-          k_new, v_new, kc, vc, slots, n_tok, num_kv_heads, head_dim, page_size, num_blocks, k_scale, v_scale, err);
+          k_new, v_new, kc, vc, slots, n_tok, num_kv_heads, head_dim, page_size, num_blocks, k_scale, v_scale, scale_stride, err);
       break;
     default:
       append_kernel<kKvE5m2><<<static_cast<int>(blocks), threads, 0, stream>>>(
-          k_new, v_new, kc, vc, slots, n_tok, num_kv_heads, head_dim, page_size, num_blocks, k_scale, v_scale, err);
+          k_new, v_new, kc, vc, slots, n_tok, num_kv_heads, head_dim, page_size, num_blocks, k_scale, v_scale, scale_stride, err);
       break;
   }
   return cudaGetLastError();

@@ -229,9 +229,9 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
   const int row_base = rg * ROWS_W;
 
   float kscale = 1.f, vscale = 1.f;
-  if (KV != kKvFp16) {
-    kscale = *p.k_scale;
-    vscale = *p.v_scale;
+  if (KV != kKvFp16) {  // the pool's scale, or this KV head's
+    kscale = p.k_scale[kvh * p.scale_stride];
+    vscale = p.v_scale[kvh * p.scale_stride];
   }
   // logits in base-2 units: s2 = acc * softmax_scale * k_scale * log2(e)
   const float sc2 = p.softmax_scale * kscale * 1.4426950408889634f;

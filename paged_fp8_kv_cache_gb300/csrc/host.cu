@@ -150,6 +150,14 @@ bool valid_dtype(pfkv_kv_dtype d) {
   return d == PFKV_KV_FP16 || d == PFKV_KV_FP8_E4M3 || d == PFKV_KV_FP8_E5M2;
 }
 
+// A dtype argument is a cache format, optionally ORed with PFKV_KV_SCALES_PER_HEAD (FP8 only).
+bool split_dtype(pfkv_kv_dtype in, pfkv_kv_dtype* fmt, int* scale_stride) {
+  const unsigned v = static_cast<unsigned>(in);
+  *fmt = static_cast<pfkv_kv_dtype>(v & ~static_cast<unsigned>(PFKV_KV_SCALES_PER_HEAD));
+  *scale_stride = (v & PFKV_KV_SCALES_PER_HEAD) ? 1 : 0;
+  return valid_dtype(*fmt) && !(*scale_stride && *fmt == PFKV_KV_FP16);
+}
+
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 int log2i(int x) {
@@ -294,7 +302,8 @@ const char* pfkv_last_error(void) { return g_last_error.c_str(); }
 uint32_t pfkv_capabilities(void) {
   return PFKV_CAP_KV_FP16 | PFKV_CAP_KV_FP8_E4M3 | PFKV_CAP_KV_FP8_E5M2 | PFKV_CAP_HEAD_DIM_128 |
          PFKV_CAP_HEAD_DIM_256 | PFKV_CAP_PAGE_16 | PFKV_CAP_PAGE_2048 | PFKV_CAP_PAGE_POW2_ANY |
-         PFKV_CAP_Q_TOKENS_1_8 | PFKV_CAP_Q_TOKENS_1_16 | PFKV_CAP_SPLIT_KV;
+         PFKV_CAP_Q_TOKENS_1_8 | PFKV_CAP_Q_TOKENS_1_16 | PFKV_CAP_SPLIT_KV |
+         PFKV_CAP_SCALES_PER_HEAD;
 }
 
 pfkv_status pfkv_device_errors(uint32_t* flags, int clear) {
@@ -314,12 +323,15 @@ pfkv_status pfkv_device_errors(uint32_t* flags, int clear) {
 
 pfkv_status pfkv_kv_cache_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                                  const int64_t* slot_mapping, int n_tok, int num_kv_heads, int head_dim,
-                                 int page_size, int num_blocks, pfkv_kv_dtype dtype, const float* k_scale,
+                                 int page_size, int num_blocks, pfkv_kv_dtype dtype_arg, const float* k_scale,
                                  const float* v_scale, pfkv_stream_t stream) {
   if (n_tok < 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0 || num_blocks <= 0)
     return fail(PFKV_ERR_INVALID_ARG, "bad size (n_tok=%d Hkv=%d D=%d P=%d num_blocks=%d)", n_tok, num_kv_heads,
                 head_dim, page_size, num_blocks);
-  if (!valid_dtype(dtype)) return fail(PFKV_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(dtype));
+  pfkv_kv_dtype dtype;
+  int scale_stride;
+  if (!split_dtype(dtype_arg, &dtype, &scale_stride))
+    return fail(PFKV_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(dtype_arg));
   if (head_dim % 8 != 0 || head_dim > 1024)
     return fail(PFKV_ERR_UNSUPPORTED, "head_dim %d (must be a multiple of 8, at most 1024)", head_dim);
   if (n_tok == 0) return PFKV_OK;
@@ -336,17 +348,20 @@ pfkv_status pfkv_kv_cache_append(const void* k_new, const void* v_new, void* k_c
   if (e != cudaSuccess) return cuda_fail(e, "device set-up");
   e = launch_append(static_cast<const __half*>(k_new), static_cast<const __half*>(v_new), k_cache, v_cache,
                     slot_mapping, n_tok, num_kv_heads, head_dim, page_size, num_blocks, kv_of(dtype), k_scale, v_scale,
-                    err, reinterpret_cast<cudaStream_t>(stream));
+                    scale_stride, err, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PFKV_OK : cuda_fail(e, "append launch");
 }
 
 pfkv_status pfkv_kv_cache_zero_blocks(void* k_cache, void* v_cache, const int32_t* block_ids, int n_ids,
                                       int num_kv_heads, int head_dim, int page_size, int num_blocks,
-                                      pfkv_kv_dtype dtype, pfkv_stream_t stream) {
+                                      pfkv_kv_dtype dtype_arg, pfkv_stream_t stream) {
   if (n_ids < 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0 || num_blocks <= 0)
     return fail(PFKV_ERR_INVALID_ARG, "bad size (n_ids=%d Hkv=%d D=%d P=%d num_blocks=%d)", n_ids, num_kv_heads,
                 head_dim, page_size, num_blocks);
-  if (!valid_dtype(dtype)) return fail(PFKV_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(dtype));
+  pfkv_kv_dtype dtype;
+  int unused_stride;
+  if (!split_dtype(dtype_arg, &dtype, &unused_stride))
+    return fail(PFKV_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(dtype_arg));
   // every cache row a whole number of 16-byte stores
   const int row_bytes = head_dim * (dtype == PFKV_KV_FP16 ? 2 : 1);
   if (row_bytes % 16 != 0 || head_dim > 1024)
@@ -369,8 +384,12 @@ pfkv_status pfkv_kv_cache_zero_blocks(void* k_cache, void* v_cache, const int32_
 }
 
 pfkv_status pfkv_decode_plan(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads, int head_dim,
-                             int page_size, pfkv_kv_dtype dtype, int max_seq_len, int num_splits_request,
+                             int page_size, pfkv_kv_dtype dtype_arg, int max_seq_len, int num_splits_request,
                              int* num_splits, int* split_tokens) {
+  pfkv_kv_dtype dtype;
+  int unused_stride;
+  if (!split_dtype(dtype_arg, &dtype, &unused_stride))
+    return fail(PFKV_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(dtype_arg));
   Plan pl;
   pfkv_status st = make_plan(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype,
                              max_seq_len, num_splits_request, &pl);
@@ -381,7 +400,10 @@ pfkv_status pfkv_decode_plan(int num_seqs, int num_q_tokens, int num_q_heads, in
 }
 
 size_t pfkv_decode_workspace_bytes(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads, int head_dim,
-                                   int page_size, pfkv_kv_dtype dtype, int max_seq_len, int num_splits_request) {
+                                   int page_size, pfkv_kv_dtype dtype_arg, int max_seq_len, int num_splits_request) {
+  pfkv_kv_dtype dtype;
+  int unused_stride;
+  if (!split_dtype(dtype_arg, &dtype, &unused_stride)) return 0;
   Plan pl;
   if (make_plan(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype, max_seq_len,
                 num_splits_request, &pl) != PFKV_OK)
@@ -392,10 +414,14 @@ size_t pfkv_decode_workspace_bytes(int num_seqs, int num_q_tokens, int num_q_hea
 pfkv_status pfkv_paged_attention_decode(void* out, float* lse, const void* q, const void* k_cache, const void* v_cache,
                                         const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
                                         int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads,
-                                        int head_dim, int page_size, int num_blocks, pfkv_kv_dtype dtype,
+                                        int head_dim, int page_size, int num_blocks, pfkv_kv_dtype dtype_arg,
                                         const float* k_scale, const float* v_scale, float softmax_scale,
                                         int max_seq_len, int num_splits, void* workspace, size_t workspace_bytes,
                                         pfkv_stream_t stream) {
+  pfkv_kv_dtype dtype;
+  int scale_stride;
+  if (!split_dtype(dtype_arg, &dtype, &scale_stride))
+    return fail(PFKV_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(dtype_arg));
   Plan pl;
   pfkv_status st = make_plan(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype,
                              max_seq_len, num_splits, &pl);
@@ -443,6 +469,7 @@ pfkv_status pfkv_paged_attention_decode(void* out, float* lse, const void* q, co
   p.seq_lens = seq_lens;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
+  p.scale_stride = scale_stride;
   const size_t nrows = static_cast<size_t>(num_seqs) * num_q_tokens * num_q_heads;
   p.o_part = need ? static_cast<float*>(workspace) : nullptr;
   p.lse_part = need ? static_cast<float*>(workspace) + nrows * pl.splits * head_dim : nullptr;

@@ -26,6 +26,7 @@ struct DecodeParams {
   const int32_t* seq_lens;
   const float* k_scale;
   const float* v_scale;
+  int scale_stride;  // 0: one scale per pool; 1: one per KV head (k_scale[kvh])
   float* o_part;
   float* lse_part;
   unsigned* err;
@@ -105,7 +106,7 @@ cudaError_t launch_zero_blocks(void* k_cache, void* v_cache, const int32_t* bloc
 // append.cu
 cudaError_t launch_append(const __half* k_new, const __half* v_new, void* k_cache, void* v_cache,
                           const int64_t* slots, int n_tok, int num_kv_heads, int head_dim, int page_size,
-                          int num_blocks, int kv, const float* k_scale, const float* v_scale, unsigned* err,
-                          cudaStream_t stream);
+                          int num_blocks, int kv, const float* k_scale, const float* v_scale, int scale_stride,
+                          unsigned* err, cudaStream_t stream);
 
 }  // namespace pfkv

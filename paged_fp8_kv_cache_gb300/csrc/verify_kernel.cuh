@@ -314,7 +314,8 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
                  "r"(S::TMEM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  const float kscale = *p.k_scale, vscale = *p.v_scale;
+  // the pool's scale, or this KV head's
+  const float kscale = p.k_scale[kvh * p.scale_stride], vscale = p.v_scale[kvh * p.scale_stride];
   const float sc2 = p.softmax_scale * kscale * 1.4426950408889634f;
   // Q -> three E4M3 terms in shared memory (K-major, 128B swizzle), one warp per row; padded rows zero
   {

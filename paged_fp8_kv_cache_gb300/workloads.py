@@ -26,7 +26,11 @@ and rounded to fp16 (round-to-nearest-even).
 * Scales: ``k_scale = float32(amax|K16| / fmt_max)`` over every K value of
   the workload (cached and appended), fmt_max 448 (E4M3) or 57344 (E5M2);
   likewise ``v_scale``; 1.0 for an fp16 cache. ``softmax_scale =
-  float32(1/sqrt(D))``.
+  float32(1/sqrt(D))``. With ``scale_per_head`` the amax runs over each KV
+  head's values alone and the scales are float32 arrays ``[Hkv]``.
+* Head gains (``head_gain``, a tuple cycled over the KV heads): K and V of KV
+  head h are multiplied by ``head_gain[h % len]`` in float32 before the fp16
+  rounding (after the outliers), so that heads differ in magnitude.
 """
 
 from __future__ import annotations
@@ -56,6 +60,8 @@ class CaseSpec:
     pool_factor: float = 1.0
     append_new: int = 0
     seed: int = 0
+    scale_per_head: bool = False
+    head_gain: tuple = ()
 
 
 # The five workloads of the benchmark (seed = 1000 + workload id).
@@ -82,11 +88,17 @@ CONFIGS = {
 
 # Workloads of rows built beyond the five, measured with the same harness and reported apart:
 # a q16 verify (15 drafts + 1) at 256K keys, the q8 verifier's shape class with 16 query tokens
-# per sequence and 4 query heads per KV head (64 rows per KV head).
+# per sequence and 4 query heads per KV head (64 rows per KV head); and the 128K decode with
+# one static scale per KV head over heads of different magnitude.
 EXTENSIONS = {
     6: CaseSpec("q16 speculative verify: 2 seqs x 262144, q16 causal, Hq16/Hkv4, D256, E5M2 KV, page 2048",
                 contexts=(262144,) * 2, num_q_tokens=16, num_q_heads=16, num_kv_heads=4,
                 head_dim=256, page_size=2048, kv_dtype="e5m2", seed=1006),
+    7: CaseSpec("long-context decode with one scale per KV head: 1 seq x 131072, q1, Hq24/Hkv4, D256, E4M3 KV, "
+                "page 2048, KV heads of magnitude x0.25/x1/x4/x0.5",
+                contexts=(131072,), num_q_tokens=1, num_q_heads=24, num_kv_heads=4,
+                head_dim=256, page_size=2048, kv_dtype="e4m3", v_dist="uniform",
+                k_outlier_frac=0.01, seed=1007, scale_per_head=True, head_gain=(0.25, 1.0, 4.0, 0.5)),
 }
 
 ALL = {**CONFIGS, **EXTENSIONS}
@@ -175,13 +187,23 @@ def make_case(spec: CaseSpec, seed: int | None = None) -> Case:
         rows = rng.choice(n_fill * Hkv, size=n_rows, replace=False)
         kr = k.reshape(n_fill * Hkv, D)
         kr[rows] *= np.float32(spec.k_outlier_mul)
+    gain = None
+    if spec.head_gain:
+        gain = np.array([spec.head_gain[h % len(spec.head_gain)] for h in range(Hkv)], np.float32)[:, None]
+        k *= gain
+        v *= gain
     k16 = k.astype(np.float16)
     v16 = v.astype(np.float16)
     del k, v
     # 7. new tokens
     n_new = B * spec.append_new
-    k_new = rng.standard_normal((n_new, Hkv, D), dtype=np.float32).astype(np.float16)
-    v_new = rng.standard_normal((n_new, Hkv, D), dtype=np.float32).astype(np.float16)
+    k_new = rng.standard_normal((n_new, Hkv, D), dtype=np.float32)
+    v_new = rng.standard_normal((n_new, Hkv, D), dtype=np.float32)
+    if gain is not None:
+        k_new *= gain
+        v_new *= gain
+    k_new = k_new.astype(np.float16)
+    v_new = v_new.astype(np.float16)
 
     def slots_for(b: int, positions: np.ndarray) -> np.ndarray:
         return block_table[b, positions // P].astype(np.int64) * P + positions % P
@@ -192,6 +214,19 @@ def make_case(spec: CaseSpec, seed: int | None = None) -> Case:
 
     if spec.kv_dtype == "fp16":
         k_scale = v_scale = np.float32(1.0)
+    elif spec.scale_per_head:
+        fmax = FMT_MAX[spec.kv_dtype]
+
+        def head_amax(a, b):
+            out = np.zeros(Hkv)
+            for arr in (a, b):
+                if arr.shape[0]:
+                    out = np.maximum(out, np.abs(arr).max(axis=(0, 2)).astype(np.float64))
+            return out
+
+        ka, va = head_amax(k16, k_new), head_amax(v16, v_new)
+        k_scale = np.where(ka > 0, ka / fmax, 1.0).astype(np.float32)
+        v_scale = np.where(va > 0, va / fmax, 1.0).astype(np.float32)
     else:
         fmax = FMT_MAX[spec.kv_dtype]
         kam = max(float(np.abs(k16).max()) if n_fill else 0.0, float(np.abs(k_new).max()) if n_new else 0.0)

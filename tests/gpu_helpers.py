@@ -25,8 +25,9 @@ class GpuCase:
         shape = (case.num_blocks, s.num_kv_heads, s.page_size, s.head_dim)
         self.k_cache = torch.zeros(shape, dtype=elt, device=DEV)
         self.v_cache = torch.zeros(shape, dtype=elt, device=DEV)
-        self.k_scale = torch.tensor([float(case.k_scale)], dtype=torch.float32, device=DEV)
-        self.v_scale = torch.tensor([float(case.v_scale)], dtype=torch.float32, device=DEV)
+        # one float per pool, or one per KV head (the binding then sets PFKV_KV_SCALES_PER_HEAD)
+        self.k_scale = torch.tensor(np.asarray(case.k_scale, np.float32).reshape(-1), device=DEV)
+        self.v_scale = torch.tensor(np.asarray(case.v_scale, np.float32).reshape(-1), device=DEV)
         self.q = to_dev(case.q)
         self.block_table = to_dev(case.block_table)
         self.seq_lens = to_dev(case.seq_lens)

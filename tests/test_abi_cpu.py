@@ -139,3 +139,24 @@ def test_zero_blocks_rejects_rows_of_partial_16_byte_stores(pflib):
     # FP8 rows of 8 bytes (head_dim 8) would need an 8-byte tail store: unsupported; fp16 rows of 16 bytes are fine
     assert lib.pfkv_kv_cache_zero_blocks(None, None, None, 4, 1, 8, 1, 10, 1, None) == pf.PFKV_ERR_UNSUPPORTED
     assert lib.pfkv_kv_cache_zero_blocks(None, None, None, 4, 1, 8, 1, 10, 0, None) == pf.PFKV_ERR_INVALID_ARG
+
+
+def test_per_head_scale_flag_on_the_host(pflib):
+    lib = pf.load()
+    per_head = pf.PFKV_KV_SCALES_PER_HEAD
+    assert pf.pfkv_capabilities() & 0x8000
+    # plan and workspace accept and ignore the flag
+    assert pf.pfkv_decode_plan(2, 1, 24, 4, 256, 2048, 1 | per_head, 131072, 38) == \
+        pf.pfkv_decode_plan(2, 1, 24, 4, 256, 2048, 1, 131072, 38)
+    assert pf.pfkv_decode_workspace_bytes(2, 1, 24, 4, 256, 2048, 2 | per_head, 131072, 38) == \
+        pf.pfkv_decode_workspace_bytes(2, 1, 24, 4, 256, 2048, 2, 131072, 38) > 0
+    # with an fp16 cache the flag is an invalid argument (there is no scale)
+    assert lib.pfkv_kv_cache_append(None, None, None, None, None, 4, 8, 128, 16, 10, 0 | per_head, None, None,
+                                    None) == pf.PFKV_ERR_INVALID_ARG
+    assert "dtype" in pf.pfkv_last_error()
+    with pytest.raises(pf.PfkvError) as ei:
+        pf.pfkv_decode_plan(2, 1, 24, 4, 256, 2048, 0 | per_head, 4096, 2)
+    assert ei.value.status == pf.PFKV_ERR_INVALID_ARG
+    # an unknown format with the flag is still unknown
+    assert lib.pfkv_kv_cache_append(None, None, None, None, None, 4, 8, 128, 16, 10, 3 | per_head, None, None,
+                                    None) == pf.PFKV_ERR_INVALID_ARG

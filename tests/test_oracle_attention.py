@@ -22,6 +22,7 @@ import numpy as np
 import pytest
 
 import oracle.attention as oatt
+from oracle import append as oappend
 from oracle import fp8, merge
 from paged_fp8_kv_cache_gb300 import workloads
 from tests.oracle_helpers import oracle_caches
@@ -47,7 +48,9 @@ def brute(case, kc, vc):
     s = case.spec
     T, Hq, Hkv, D, P = s.num_q_tokens, s.num_q_heads, s.num_kv_heads, s.head_dim, s.page_size
     g = Hq // Hkv
-    ks, vs, sm = float(case.k_scale), float(case.v_scale), float(case.softmax_scale)
+    sm = float(case.softmax_scale)
+    ksa = np.asarray(case.k_scale, dtype=np.float32).reshape(-1)
+    vsa = np.asarray(case.v_scale, dtype=np.float32).reshape(-1)
 
     def val(cache, page, kvh, off, d):
         x = cache[page, kvh, off, d]
@@ -60,6 +63,8 @@ def brute(case, kc, vc):
         for t in range(T):
             for h in range(Hq):
                 kvh = h // g
+                ks = float(ksa[kvh % ksa.size])  # one scale per pool, or KV head kvh's
+                vs = float(vsa[kvh % vsa.size])
                 qv = [float(case.q[b * T + t, h, d]) for d in range(D)]
                 keys = list(range(0, n - T + t + 1))
                 if not keys:
@@ -88,6 +93,8 @@ BRUTE_CASES = [
     dict(kv="e4m3", T=3, g=1, D=4, P=16, contexts=(33,), Hkv=3),
     dict(kv="e5m2", T=1, g=2, D=8, P=4, contexts=(40, 17), v_dist="uniform", k_outlier_frac=0.1),
     dict(kv="e4m3", T=16, g=2, D=4, P=4, contexts=(21, 16)),  # q16 verify: 15 drafts + 1
+    # one scale per KV head, heads of different magnitude
+    dict(kv="e5m2", T=2, g=2, Hkv=3, D=8, P=4, contexts=(25, 9), scale_per_head=True, head_gain=(0.25, 4.0, 1.0)),
 ]
 
 
@@ -289,3 +296,39 @@ def test_merge_closed_forms():
     mo1, ml1 = merge.lse_merge(o, lse)
     mo2, ml2 = merge.lse_merge(o, lse + 3.0)
     assert np.allclose(mo1, mo2) and np.allclose(ml2, ml1 + 3.0)
+
+
+@pytest.mark.parametrize("kv", ["e4m3", "e5m2"])
+def test_per_head_scales_all_equal_reduce_to_the_per_tensor_scale(kv):
+    # one scale per KV head, all equal to the pool's scale: the same cache bytes and the same
+    # attention as the per-tensor scale, exactly
+    case = workloads.make_case(tiny_spec(kv, T=3, g=2, Hkv=3, P=4, contexts=(23, 30)))
+    Hkv = case.spec.num_kv_heads
+    kc, vc = oracle_caches(case)
+    ks = np.full(Hkv, case.k_scale, np.float32)
+    vs = np.full(Hkv, case.v_scale, np.float32)
+    kc2, vc2 = np.zeros_like(kc), np.zeros_like(vc)
+    oappend.append_bulk(kc2, case.k_fill, case.slot_fill, case.spec.page_size, ks, kv)
+    oappend.append_bulk(vc2, case.v_fill, case.slot_fill, case.spec.page_size, vs, kv)
+    assert np.array_equal(kc, kc2) and np.array_equal(vc, vc2)
+    o1, l1 = run(oatt.paged_attention, case, kc, vc)
+    o2, l2 = run(oatt.paged_attention, case, kc2, vc2, k_scale=ks, v_scale=vs)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("kv", ["e4m3", "e5m2"])
+def test_per_head_scale_commutes_with_power_of_two_head_gains(kv):
+    # multiplying KV head h's fp16 values and its scale by the same power of two leaves its FP8
+    # bytes unchanged (the float32 quotient is the same number), so each head is quantised
+    # against its own scale only
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((50, 3, 16)).astype(np.float16)
+    s = np.array([0.01, 0.02, 0.005], np.float32)
+    gains = np.array([1.0, 2.0, 8.0], np.float32)
+    a = oappend.quantise(x, oappend.head_scales(s, 3), kv)
+    b = oappend.quantise((x.astype(np.float32) * gains[:, None]).astype(np.float16),
+                         oappend.head_scales(s * gains, 3), kv)
+    assert np.array_equal(a, b)
+    # and a head quantised alone with its scale gives the same bytes
+    for h in range(3):
+        assert np.array_equal(a[:, h], oappend.quantise(x[:, h], s[h], kv))
