@@ -1,7 +1,13 @@
 """One static scale per KV head (PFKV_KV_SCALES_PER_HEAD) on KV heads of different magnitude:
 the appended FP8 bytes bit-exact against the oracle, and attention within tolerance on both
 kernels (mma.sync decode kernel, tcgen05 grouped verifier), with the automatic split plan and
-explicit ranges; and the per-tensor call on the same cache bytes as a cross-check of the flag."""
+explicit ranges; and the per-tensor call on the same cache bytes as a cross-check of the flag.
+
+The tolerances are the unit-scale ones (2e-3 on the fp16 output, 1e-4 on the LSE) taken in each
+head's own units: KV head h's K and V are its unit-scale values times gain_h, so its outputs are
+gain_h times larger (and so is their fp16 rounding) and its logits gain_h times larger (and so is
+the rounding of their fp32 sums); outputs are compared after dividing by gain_h, LSEs against
+1e-4 * max(1, gain_h)."""
 
 import numpy as np
 import pytest
@@ -9,7 +15,7 @@ import torch
 
 from paged_fp8_kv_cache_gb300 import binding as pf
 from paged_fp8_kv_cache_gb300 import workloads
-from tests.gpu_helpers import GpuCase, assert_close
+from tests.gpu_helpers import GpuCase
 from tests.oracle_helpers import oracle_attention, oracle_caches
 
 pytestmark = pytest.mark.gpu
@@ -44,10 +50,19 @@ def test_per_head_scales(kv, D, T, g, hkv, P):
     torch.cuda.synchronize()
     assert np.array_equal(gc.k_cache.cpu().numpy(), kc)
     assert np.array_equal(gc.v_cache.cpu().numpy(), vc)
+    gain = np.array([GAINS[(h // g) % len(GAINS)] for h in range(g * hkv)])  # of query head h's KV head
     for splits in (0, 3):
         out, lse = gc.decode(num_splits=splits)
         torch.cuda.synchronize()
-        assert_close(out, lse, o_ref, l_ref)
+        o = out.float().cpu().numpy().astype(np.float64)
+        l = lse.cpu().numpy().astype(np.float64)
+        ok = np.isfinite(l_ref)
+        assert np.array_equal(np.isneginf(l), np.isneginf(l_ref))
+        assert np.all(o[~ok] == 0)
+        do = np.abs((o - o_ref) / gain[None, :, None]).max()
+        dl = (np.abs(l - l_ref) / np.maximum(1.0, gain)[None, :])[ok].max()
+        assert do <= 2e-3, f"max |out - oracle| / gain = {do:.3e}"
+        assert dl <= 1e-4, f"max |lse - oracle| / max(1, gain) = {dl:.3e}"
 
 
 def test_per_head_flag_with_equal_scales_matches_per_tensor():
