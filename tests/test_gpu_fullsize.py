@@ -1,10 +1,12 @@
-"""The five benchmark workloads at full size, in the launch configuration the
-benchmark times (automatic split plan), checked against the oracle.
+"""The five benchmark workloads and the extension workloads (q16 verify, one scale per KV
+head) at full size, in the launch configuration the benchmark times (automatic split plan),
+checked against the oracle.
 
 The oracle computes whole (sequence, KV head) units; for the large
 workloads a seeded sample of units is checked (every row and head-dim
 element of each sampled unit), and cache bytes are compared on a seeded
-sample of tokens.
+sample of tokens. With one scale per KV head (heads of different magnitude) the tolerances are
+taken in each head's units: outputs divided by the head's gain, LSEs against 1e-4 * max(1, gain).
 """
 
 import numpy as np
@@ -19,7 +21,7 @@ from tests.oracle_helpers import oracle_attention
 
 pytestmark = pytest.mark.gpu
 
-UNITS_CHECKED = {1: None, 2: None, 3: None, 4: 2, 5: 6}
+UNITS_CHECKED = {1: None, 2: None, 3: None, 4: 2, 5: 6, 6: 2, 7: None}
 
 
 @pytest.fixture(autouse=True)
@@ -41,9 +43,9 @@ def _gather_cache(gpu_cache, case, units):
     return host
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, 6, 7])
 def test_full_size_workload(cfg):
-    case = workloads.make_case(workloads.CONFIGS[cfg])
+    case = workloads.make_case(workloads.ALL[cfg])
     s = case.spec
     g = GpuCase(case)
     out, lse = g.decode()
@@ -64,8 +66,10 @@ def test_full_size_workload(cfg):
         assert np.array_equal(got_k.view(np.uint16), all_k[pick].view(np.uint16))
         assert np.array_equal(got_v.view(np.uint16), all_v[pick].view(np.uint16))
     else:
-        assert np.array_equal(got_k, oappend.quantise(all_k[pick], case.k_scale, s.kv_dtype))
-        assert np.array_equal(got_v, oappend.quantise(all_v[pick], case.v_scale, s.kv_dtype))
+        ks = oappend.head_scales(case.k_scale, s.num_kv_heads)
+        vs = oappend.head_scales(case.v_scale, s.num_kv_heads)
+        assert np.array_equal(got_k, oappend.quantise(all_k[pick], ks, s.kv_dtype))
+        assert np.array_equal(got_v, oappend.quantise(all_v[pick], vs, s.kv_dtype))
 
     # attention: every unit (small workloads) or a seeded sample of units
     all_units = [(b, h) for b in range(case.B) for h in range(s.num_kv_heads)]
@@ -80,8 +84,11 @@ def test_full_size_workload(cfg):
         rows[b * T:(b + 1) * T, kvh * g_:(kvh + 1) * g_] = True
     o = out.float().cpu().numpy().astype(np.float64)
     l = lse.cpu().numpy().astype(np.float64)
-    do = np.abs(o[rows] - o_ref[rows]).max()
-    dl = np.abs(l[rows] - l_ref[rows]).max()
+    # each query head's KV-head gain (1 without head gains)
+    hg = s.head_gain or (1.0,)
+    gain = np.array([hg[(h // g_) % len(hg)] for h in range(s.num_q_heads)])[None, :].repeat(o.shape[0], 0)
+    do = (np.abs(o - o_ref) / gain[:, :, None])[rows].max()
+    dl = (np.abs(l - l_ref) / np.maximum(1.0, gain))[rows].max()
     assert do <= 2e-3, f"max |out - oracle| = {do:.3e}"
     assert dl <= 1e-4, f"max |lse - oracle| = {dl:.3e}"
     # every row is finite (all sequences are non-empty)
