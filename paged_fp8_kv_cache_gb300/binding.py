@@ -123,10 +123,14 @@ def _kv(dtype) -> int:
     return KV_DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
 
 
-def _kv_scaled(dtype, k_scale) -> int:
+def _kv_scaled(dtype, k_scale, v_scale, num_kv_heads) -> int:
     """The dtype argument, with PFKV_KV_SCALES_PER_HEAD when the scale tensors hold one float per KV head."""
     kv = _kv(dtype)
-    if k_scale is not None and k_scale.numel() > 1:
+    n = [t.numel() for t in (k_scale, v_scale) if t is not None]
+    if n and max(n) > 1:
+        if any(x != num_kv_heads for x in n):
+            raise PfkvError(PFKV_ERR_INVALID_ARG, f"scales of {n} floats: one per pool or one per KV head "
+                                                  f"({num_kv_heads}) expected")
         kv |= PFKV_KV_SCALES_PER_HEAD
     return kv
 
@@ -145,8 +149,9 @@ def pfkv_kv_cache_append(k_new, v_new, k_cache, v_cache, slot_mapping, page_size
     lib = load()
     n_tok, hkv, d = k_new.shape
     _check(lib.pfkv_kv_cache_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping),
-                                    n_tok, hkv, d, page_size, k_cache.shape[0], _kv_scaled(kv_dtype, k_scale),
-                                    _ptr(k_scale), _ptr(v_scale), _stream(stream)))
+                                    n_tok, hkv, d, page_size, k_cache.shape[0],
+                                    _kv_scaled(kv_dtype, k_scale, v_scale, hkv), _ptr(k_scale), _ptr(v_scale),
+                                    _stream(stream)))
 
 
 def pfkv_decode_plan(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, kv_dtype,
@@ -176,8 +181,8 @@ def pfkv_paged_attention_decode(out, lse, q, k_cache, v_cache, block_table, seq_
     _check(lib.pfkv_paged_attention_decode(
         _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
         _ptr(seq_lens), num_seqs, num_q_tokens, hq, num_kv_heads, d, page_size, k_cache.shape[0],
-        _kv_scaled(kv_dtype, k_scale), _ptr(k_scale), _ptr(v_scale), float(softmax_scale), max_seq_len, num_splits,
-        _ptr(workspace), ws_bytes,
+        _kv_scaled(kv_dtype, k_scale, v_scale, num_kv_heads), _ptr(k_scale), _ptr(v_scale), float(softmax_scale),
+        max_seq_len, num_splits, _ptr(workspace), ws_bytes,
         _stream(stream)))
 
 
@@ -191,8 +196,8 @@ def pfkv_paged_attention_decode_static_scratch(out, lse, q, k_cache, v_cache, bl
     _check(lib.pfkv_paged_attention_decode_static_scratch(
         _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
         _ptr(seq_lens), num_seqs, num_q_tokens, hq, num_kv_heads, d, page_size, k_cache.shape[0],
-        _kv_scaled(kv_dtype, k_scale), _ptr(k_scale), _ptr(v_scale), float(softmax_scale), max_seq_len, num_splits,
-        _stream(stream)))
+        _kv_scaled(kv_dtype, k_scale, v_scale, num_kv_heads), _ptr(k_scale), _ptr(v_scale), float(softmax_scale),
+        max_seq_len, num_splits, _stream(stream)))
 
 
 def pfkv_lse_merge(out, lse, o_parts, lse_parts, stream=None):

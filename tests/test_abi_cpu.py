@@ -160,3 +160,15 @@ def test_per_head_scale_flag_on_the_host(pflib):
     # an unknown format with the flag is still unknown
     assert lib.pfkv_kv_cache_append(None, None, None, None, None, 4, 8, 128, 16, 10, 3 | per_head, None, None,
                                     None) == pf.PFKV_ERR_INVALID_ARG
+
+
+def test_binding_sets_the_per_head_flag_from_the_scale_tensors():
+    import torch
+    one, four, three = torch.ones(1), torch.ones(4), torch.ones(3)
+    assert pf._kv_scaled("e4m3", one, one, 4) == pf.PFKV_KV_FP8_E4M3
+    assert pf._kv_scaled("e5m2", four, four, 4) == pf.PFKV_KV_FP8_E5M2 | pf.PFKV_KV_SCALES_PER_HEAD
+    assert pf._kv_scaled("fp16", None, None, 4) == pf.PFKV_KV_FP16
+    for k, v in ((three, three), (four, one), (one, four)):  # a count that is neither 1 nor num_kv_heads
+        with pytest.raises(pf.PfkvError) as ei:
+            pf._kv_scaled("e4m3", k, v, 4)
+        assert ei.value.status == pf.PFKV_ERR_INVALID_ARG
