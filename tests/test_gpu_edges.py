@@ -6,7 +6,7 @@ import torch
 
 from paged_fp8_kv_cache_gb300 import binding as pf
 from paged_fp8_kv_cache_gb300 import workloads
-from tests.gpu_helpers import GpuCase, assert_close, to_dev
+from tests.gpu_helpers import GpuCase, assert_close
 from tests.oracle_helpers import oracle_attention, oracle_caches
 
 pytestmark = pytest.mark.gpu

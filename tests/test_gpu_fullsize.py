@@ -16,7 +16,7 @@ import torch
 from oracle import append as oappend
 from paged_fp8_kv_cache_gb300 import binding as pf
 from paged_fp8_kv_cache_gb300 import workloads
-from tests.gpu_helpers import GpuCase, assert_close
+from tests.gpu_helpers import GpuCase
 from tests.oracle_helpers import oracle_attention
 
 pytestmark = pytest.mark.gpu

@@ -3,7 +3,6 @@ ranges and their LSE merge, checked against the oracle when the workspace
 starts out holding garbage, when one workspace serves calls with different
 split counts, and when the call is replayed from a captured CUDA graph."""
 
-import numpy as np
 import pytest
 import torch
 

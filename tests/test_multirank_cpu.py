@@ -1,6 +1,5 @@
 """The multi-rank (replica) host logic of bench.py with 2 gloo ranks on CPU."""
 
-import os
 import socket
 
 import pytest

@@ -10,7 +10,6 @@ in a row, and passes both alone in a fresh process and after every other
 test.
 """
 
-import numpy as np
 import pytest
 import torch
 
