@@ -257,6 +257,9 @@ MUTANTS = {
     "log base 2 in lse": ("m + np.log(np.where(has, L, 1.0))", "m + np.log2(np.where(has, L, 1.0))"),
     "missing max subtraction in weights": ("w = np.exp(s - np.where(has, m, 0.0)[:, None])", "w = np.exp(s)"),
     "no normalisation": ("acc / np.where(has, L, 1.0)[:, None]", "acc"),
+    "per-head scales: head 0's for every head": ("ks = ks_all[kvh if ks_all.size > 1 else 0]", "ks = ks_all[0]"),
+    "per-head scales: K's scale for V": ("vs = vs_all[kvh if vs_all.size > 1 else 0]",
+                                         "vs = ks_all[kvh if ks_all.size > 1 else 0]"),
 }
 
 
