@@ -17,6 +17,7 @@
 #include <vector>
 
 #include "frag_layout.h"
+#include "verify_layout.h"
 
 using namespace pfkv;
 
@@ -142,10 +143,49 @@ static void check_small_pages() {
     }
 }
 
+// The grouped verifier's P^T buffer (verify_layout.h), for 32, 48 and 64 padded rows:
+//  * (row, key) -> byte offset is a bijection onto the buffer's 2 x nmax x 128 bytes;
+//  * the softmax threads' hoisted addressing holds: for rbase in {0, nmax/2} and c a multiple of
+//    8, row rbase + c + j of a key is its row rbase + j shifted by c * 128 bytes (the swizzle
+//    phase of a row is its index mod 8);
+//  * one warp's stores of one row (32 consecutive keys of a 64-key block) touch 16 distinct
+//    4-byte banks, two lanes per word: one shared-memory wavefront.
+static void check_pt_layout() {
+  for (int nmax : {32, 48, 64}) {
+    const int bytes = 2 * nmax * 128;
+    std::vector<int> seen(bytes / 2, 0);
+    for (int row = 0; row < nmax; ++row)
+      for (int key = 0; key < 128; ++key) {
+        const int off = pt_elem(nmax, row, key);
+        CHECK(off >= 0 && off + 2 <= bytes && off % 2 == 0, "P^T nmax %d: (row %d, key %d) at %d", nmax, row, key,
+              off);
+        CHECK(seen[off / 2]++ == 0, "P^T nmax %d: (row %d, key %d) reuses byte %d", nmax, row, key, off);
+      }
+    for (int rbase : {0, nmax / 2})
+      for (int key = 0; key < 128; ++key)
+        for (int c = 0; c < nmax / 2; c += 8)
+          for (int j = 0; j < 8; ++j)
+            CHECK(pt_elem(nmax, rbase + c + j, key) == pt_elem(nmax, rbase + j, key) + 128 * c,
+                  "P^T nmax %d: hoisted address of row %d, key %d", nmax, rbase + c + j, key);
+    for (int row = 0; row < nmax; ++row)
+      for (int first = 0; first < 128; first += 32) {
+        std::set<int> words, banks;
+        for (int lane = 0; lane < 32; ++lane) {
+          const int w = pt_elem(nmax, row, first + lane) / 4;
+          words.insert(w);
+          banks.insert(w % 32);
+        }
+        CHECK(words.size() == 16 && banks.size() == 16, "P^T nmax %d: row %d keys %d.. span %zu words, %zu banks",
+              nmax, row, first, words.size(), banks.size());
+      }
+  }
+}
+
 int main() {
   for (int elt = 1; elt <= 2; ++elt)
     for (int D : {128, 256}) check_layout(elt, D);
   check_small_pages();
+  check_pt_layout();
   if (g_fail) return 1;
   std::printf("layout ok\n");
   return 0;

@@ -52,6 +52,7 @@
 #include "device_utils.cuh"
 #include "frag_layout.h"
 #include "pfkv_internal.h"
+#include "verify_layout.h"
 
 namespace pfkv {
 
@@ -175,11 +176,6 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// byte offset of 16-bit element (row, k) in a K-major 128B-swizzled block of 64-element rows
-__device__ __forceinline__ int sw128_elem(int row, int k) {
-  return row * 128 + ((((k >> 3) ^ row) & 7) << 4) + ((k & 7) << 1);
-}
 
 template <bool B>
 struct BoolTag {
