@@ -406,6 +406,8 @@ def per_config(torch, pf, flush, skip, peak, args, configs):
         res[str(cid)] = {"workload": spec.name, "GB/s": round(nb * k / (total_ms * 1e-3) / 1e9, 1),
                          "ms_per_step": round(total_ms / k, 5), "decode_call_GB/s": round(db / (dec_avg * 1e-3) / 1e9, 1),
                          "frac_of_peak": round(db / (dec_avg * 1e-3) / 1e9 / peak, 4),
+                         # the same from the median call (robust to a slow outlier call)
+                         "decode_call_GB/s_median": round(db / (statistics.median(dec) * 1e-3) / 1e9, 1),
                          "num_splits": dw.splits, "steps": k}
         del dw, case
         torch.cuda.empty_cache()
