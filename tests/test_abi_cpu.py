@@ -172,3 +172,27 @@ def test_binding_sets_the_per_head_flag_from_the_scale_tensors():
         with pytest.raises(pf.PfkvError) as ei:
             pf._kv_scaled("e4m3", k, v, 4)
         assert ei.value.status == pf.PFKV_ERR_INVALID_ARG
+
+
+def test_header_is_plain_c_and_links_against_the_library(tmp_path, pflib):
+    # the boundary is a C ABI: the header compiles as strict C99 and a C program links and calls it
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "abi.c"
+    src.write_text(
+        '#include "pfkv.h"\n'
+        "#include <stdio.h>\n"
+        "int main(void) {\n"
+        "  pfkv_kv_dtype d = (pfkv_kv_dtype)(PFKV_KV_FP8_E4M3 | PFKV_KV_SCALES_PER_HEAD);\n"
+        "  int ns = 0, st = 0;\n"
+        "  pfkv_status s = pfkv_decode_plan(4, 1, 32, 8, 128, 16, d, 4096, 13, &ns, &st);\n"
+        '  printf("%d %d %d %s\\n", (int)s, ns, st, pfkv_status_string(s));\n'
+        "  return s != PFKV_OK || (pfkv_capabilities() & PFKV_CAP_SCALES_PER_HEAD) == 0;\n"
+        "}\n")
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(pf.LIB_PATH)
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), "-L", libdir, "-lpfkv", f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    assert out[0] == "0" and out[1] == "13" and int(out[2]) * 13 >= 4096 and out[3] == "PFKV_OK"
