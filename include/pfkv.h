@@ -267,8 +267,9 @@ PFKV_API pfkv_status pfkv_paged_attention_decode(void* out, float* lse, const vo
  *    32 MiB (33554432 bytes) the call returns PFKV_ERR_WORKSPACE and enqueues
  *    nothing. The workloads of this library need at most about 16 MB.
  *  - Set-up: the first call on each device looks up the array's device
- *    address (cudaGetSymbolAddress, with that device current) and caches it;
- *    make that first call before any stream capture.
+ *    address (cudaGetSymbolAddress, with that device current) and caches it
+ *    (a call after cudaDeviceReset, in the device's new context, looks it up
+ *    again); make that first call before any stream capture.
  *  - Sharing: every call on a device uses the same array, and it keeps the
  *    last call's contents (nothing in it needs to start at zero). Calls whose
  *    work overlaps on the GPU (other streams, or another thread's calls)

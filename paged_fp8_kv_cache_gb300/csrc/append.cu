@@ -88,11 +88,12 @@ __global__ void __launch_bounds__(256) append_kernel(const __half* __restrict__ 
 cudaError_t launch_append(const __half* k_new, const __half* v_new, void* k_cache, void* v_cache, const int64_t* slots,
                           int n_tok, int num_kv_heads, int head_dim, int page_size, int num_blocks, int kv,
                           const float* k_scale, const float* v_scale, int scale_stride, unsigned* err,
-                          cudaStream_t stream) {
+                          int num_sms, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(n_tok) * num_kv_heads * (head_dim / 8);
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
-  if (blocks > 152 * 64) blocks = 152 * 64;  // grid-stride beyond ~64 CTAs per SM
+  const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 64;
+  if (blocks > cap) blocks = cap;  // grid-stride beyond 64 CTAs per SM
   if (blocks < 1) blocks = 1;
   auto* kc = static_cast<unsigned char*>(k_cache);
   auto* vc = static_cast<unsigned char*>(v_cache);

@@ -43,7 +43,10 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int g_sm_count[kMaxDevices];
 unsigned* g_err_ptr[kMaxDevices];
+unsigned long long g_err_ctx[kMaxDevices];  // context the cached error-word address belongs to
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
 
 struct TmKey {
   const void* ptr;
@@ -81,13 +84,38 @@ cudaError_t sm_count(int dev, int* n) {
   return cudaSuccess;
 }
 
-cudaError_t err_word(int dev, unsigned** p) {
+// Unique id of the current CUDA context (0 if the driver cannot tell). A device symbol's address
+// belongs to the context the module was loaded in: after cudaDeviceReset the device gets a new
+// primary context, and addresses cached for the old one must be looked up again.
+unsigned long long context_id() {
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_err_ptr[dev] == nullptr) {
+  if (g_ctx_current == nullptr || g_ctx_id == nullptr) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 4000, cudaEnableDefault, &q1) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess)
+      return 0;
+    g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f1);
+    g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f2);
+  }
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_current(&c) != CUDA_SUCCESS || c == nullptr || g_ctx_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+cudaError_t err_word(int dev, unsigned** p) {
+  const unsigned long long ctx = context_id();
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_err_ptr[dev] == nullptr || g_err_ctx[dev] != ctx) {
     void* a = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&a, g_pfkv_err);
     if (e != cudaSuccess) return e;
     g_err_ptr[dev] = static_cast<unsigned*>(a);
+    g_err_ctx[dev] = ctx;
   }
   *p = g_err_ptr[dev];
   return cudaSuccess;
@@ -341,14 +369,15 @@ pfkv_status pfkv_kv_cache_append(const void* k_new, const void* v_new, void* k_c
   if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) |
        reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15)
     return fail(PFKV_ERR_INVALID_ARG, "K/V and cache pointers must be 16-byte aligned");
-  int dev;
+  int dev, sms;
   unsigned* err;
   cudaError_t e = current_device(&dev);
   if (e == cudaSuccess) e = err_word(dev, &err);
+  if (e == cudaSuccess) e = sm_count(dev, &sms);
   if (e != cudaSuccess) return cuda_fail(e, "device set-up");
   e = launch_append(static_cast<const __half*>(k_new), static_cast<const __half*>(v_new), k_cache, v_cache,
                     slot_mapping, n_tok, num_kv_heads, head_dim, page_size, num_blocks, kv_of(dtype), k_scale, v_scale,
-                    scale_stride, err, reinterpret_cast<cudaStream_t>(stream));
+                    scale_stride, err, sms, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PFKV_OK : cuda_fail(e, "append launch");
 }
 
@@ -545,20 +574,24 @@ namespace {
 constexpr size_t kPfkvStaticScratchBytes = size_t(32) << 20;  // 32 MiB
 static __device__ __align__(256) unsigned char g_pfkv_static_scratch[kPfkvStaticScratchBytes];
 void* g_static_scratch_ptr[kMaxDevices];
+unsigned long long g_static_scratch_ctx[kMaxDevices];
 
 // Device address of the array on the current device. In host code the
 // array's name is only a host-side stand-in, never a device address: it is
-// looked up once per device (with that device current) and cached.
+// looked up once per device (with that device current) and cached, and looked
+// up again if the device's context changed since (after a cudaDeviceReset).
 pfkv_status static_scratch_address(void** out) {
   int dev;
   cudaError_t e = current_device(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const unsigned long long ctx = context_id();
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_static_scratch_ptr[dev] == nullptr) {
+  if (g_static_scratch_ptr[dev] == nullptr || g_static_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_pfkv_static_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
     g_static_scratch_ptr[dev] = p;
+    g_static_scratch_ctx[dev] = ctx;
   }
   *out = g_static_scratch_ptr[dev];
   return PFKV_OK;

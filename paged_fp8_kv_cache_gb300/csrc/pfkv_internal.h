@@ -107,6 +107,6 @@ cudaError_t launch_zero_blocks(void* k_cache, void* v_cache, const int32_t* bloc
 cudaError_t launch_append(const __half* k_new, const __half* v_new, void* k_cache, void* v_cache,
                           const int64_t* slots, int n_tok, int num_kv_heads, int head_dim, int page_size,
                           int num_blocks, int kv, const float* k_scale, const float* v_scale, int scale_stride,
-                          unsigned* err, cudaStream_t stream);
+                          unsigned* err, int num_sms, cudaStream_t stream);
 
 }  // namespace pfkv

@@ -2,26 +2,29 @@
 head) at full size, in the launch configuration the benchmark times (automatic split plan),
 checked against the oracle.
 
-The oracle computes whole (sequence, KV head) units; for the large
-workloads a seeded sample of units is checked (every row and head-dim
-element of each sampled unit), and cache bytes are compared on a seeded
-sample of tokens. With one scale per KV head (heads of different magnitude) the tolerances are
-taken in each head's units: outputs divided by the head's gain, LSEs against 1e-4 * max(1, gain).
+* Cache bytes: every byte the append kernel wrote, over every token of the workload, compared
+  chunk by chunk with the oracle's quantisation of the same fp16 inputs (read off a table of
+  the oracle's quantise over all fp16 values; see tests/oracle_helpers.py).
+* Attention: the oracle computes whole (sequence, KV head) units on its own caches (built from
+  the fp16 inputs, not from GPU bytes); every unit of the small workloads is checked, a seeded
+  sample of units of the large ones (every row and head-dim element of each sampled unit).
+With one scale per KV head (heads of different magnitude) the tolerances are taken in each
+head's units: outputs divided by the head's gain, LSEs against 1e-4 * max(1, gain).
 """
 
 import numpy as np
 import pytest
 import torch
 
-from oracle import append as oappend
 from paged_fp8_kv_cache_gb300 import binding as pf
 from paged_fp8_kv_cache_gb300 import workloads
 from tests.gpu_helpers import GpuCase
-from tests.oracle_helpers import oracle_attention
+from tests.oracle_helpers import expected_rows, head_tables, oracle_attention, unit_caches
 
 pytestmark = pytest.mark.gpu
 
-UNITS_CHECKED = {1: None, 2: None, 3: None, 4: 2, 5: 6, 6: 2, 7: None}
+UNITS_CHECKED = {1: None, 2: None, 3: None, 4: 3, 5: 64, 6: 3, 7: None}
+CHUNK_TOKENS = 1 << 15
 
 
 @pytest.fixture(autouse=True)
@@ -31,16 +34,23 @@ def _lib(pflib):
     assert pf.pfkv_device_errors(clear=True) == 0
 
 
-def _gather_cache(gpu_cache, case, units):
-    """Host copy of the pages the sampled units touch (others stay zero)."""
+def check_every_cache_byte(g, case, tables):
+    """Every token's K and V rows in the GPU pools equal the oracle's quantisation."""
     s = case.spec
-    dt = np.float16 if s.kv_dtype == "fp16" else np.uint8
-    host = np.zeros((case.num_blocks, s.num_kv_heads, s.page_size, s.head_dim), dt)
-    for b, kvh in units:
-        npg = -(-int(case.seq_lens[b]) // s.page_size)
-        pages = torch.from_numpy(case.block_table[b, :npg].astype(np.int64)).cuda()
-        host[case.block_table[b, :npg], kvh] = gpu_cache[pages, kvh].cpu().numpy()
-    return host
+    for src_k, src_v, slots in ((case.k_fill, case.v_fill, case.slot_fill),
+                                (case.k_new, case.v_new, case.slot_new)):
+        for a in range(0, slots.size, CHUNK_TOKENS):
+            sl = slots[a:a + CHUNK_TOKENS]
+            blk = torch.from_numpy(sl // s.page_size).cuda()
+            off = torch.from_numpy(sl % s.page_size).cuda()
+            got_k = g.k_cache[blk, :, off, :].cpu().numpy()
+            got_v = g.v_cache[blk, :, off, :].cpu().numpy()
+            want_k = expected_rows(src_k[a:a + CHUNK_TOKENS], tables, 0)
+            want_v = expected_rows(src_v[a:a + CHUNK_TOKENS], tables, 1)
+            if s.kv_dtype == "fp16":
+                got_k, got_v, want_k, want_v = (x.view(np.uint16) for x in (got_k, got_v, want_k, want_v))
+            assert np.array_equal(got_k, want_k), f"K cache bytes differ in tokens {a}..{a + sl.size}"
+            assert np.array_equal(got_v, want_v), f"V cache bytes differ in tokens {a}..{a + sl.size}"
 
 
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, 6, 7])
@@ -51,32 +61,15 @@ def test_full_size_workload(cfg):
     out, lse = g.decode()
     torch.cuda.synchronize()
 
-    # cache bytes: sampled tokens against the oracle's quantisation
-    rng = np.random.default_rng(cfg)
-    all_k = np.concatenate([case.k_fill, case.k_new])
-    all_v = np.concatenate([case.v_fill, case.v_new])
-    all_slots = np.concatenate([case.slot_fill, case.slot_new])
-    pick = rng.choice(all_slots.size, size=min(2048, all_slots.size), replace=False)
-    slots = all_slots[pick]
-    blk = torch.from_numpy(slots // s.page_size).cuda()
-    off = torch.from_numpy(slots % s.page_size).cuda()
-    got_k = g.k_cache[blk, :, off, :].cpu().numpy()
-    got_v = g.v_cache[blk, :, off, :].cpu().numpy()
-    if s.kv_dtype == "fp16":
-        assert np.array_equal(got_k.view(np.uint16), all_k[pick].view(np.uint16))
-        assert np.array_equal(got_v.view(np.uint16), all_v[pick].view(np.uint16))
-    else:
-        ks = oappend.head_scales(case.k_scale, s.num_kv_heads)
-        vs = oappend.head_scales(case.v_scale, s.num_kv_heads)
-        assert np.array_equal(got_k, oappend.quantise(all_k[pick], ks, s.kv_dtype))
-        assert np.array_equal(got_v, oappend.quantise(all_v[pick], vs, s.kv_dtype))
+    tables = head_tables(case)
+    check_every_cache_byte(g, case, tables)
 
-    # attention: every unit (small workloads) or a seeded sample of units
+    # attention: every unit (small workloads) or a seeded sample of units, on the oracle's caches
+    rng = np.random.default_rng(cfg)
     all_units = [(b, h) for b in range(case.B) for h in range(s.num_kv_heads)]
     n = UNITS_CHECKED[cfg]
     units = all_units if n is None else [all_units[i] for i in rng.choice(len(all_units), n, replace=False)]
-    kc = _gather_cache(g.k_cache, case, units)
-    vc = _gather_cache(g.v_cache, case, units)
+    kc, vc = unit_caches(case, units, tables)
     o_ref, l_ref = oracle_attention(case, kc, vc, units=units)
     T, g_ = s.num_q_tokens, s.num_q_heads // s.num_kv_heads
     rows = np.zeros(o_ref.shape[:2], bool)

@@ -109,3 +109,40 @@ def test_zero_blocks_clears_listed_blocks_only(kv):
         fmt = fp8.E4M3 if kv == "e4m3" else fp8.E5M2
         z = fp8.decode(np.zeros(1, np.uint8), fmt)[0]
         assert z == 0 and not np.signbit(z)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_quantise_table_lookup_is_the_oracle_call(fmt):
+    """The full-size GPU tests read the oracle's quantisation off a table of all 65536 fp16
+    inputs; a lookup must equal the direct call on any finite input."""
+    from tests.oracle_helpers import quantise_table
+    rng = np.random.default_rng(11)
+    scale = np.float32(0.0371)
+    tab = quantise_table(scale, fmt)
+    x = np.concatenate([(rng.standard_normal(20000) * 40).astype(np.float16),
+                        np.array([0.0, -0.0, 65504.0, -65504.0, 6e-8, -6e-8], np.float16)])
+    assert np.array_equal(tab[x.view(np.uint16)], append.quantise(x, scale, fmt))
+    every = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16).view(np.float16)
+    fin = np.isfinite(every)
+    assert np.array_equal(tab[fin], append.quantise(every[fin], scale, fmt))
+
+
+@pytest.mark.parametrize("cfg,heads", [(5, False), (3, True)])
+def test_unit_caches_equal_the_oracle_append(cfg, heads):
+    """Per-unit host caches built by table lookup hold the bytes oracle.append writes."""
+    from tests.oracle_helpers import head_tables, oracle_caches, unit_caches
+    over = {"contexts": ("loguniform", 30, 300, 6)} if cfg == 5 else {"contexts": (2100,)}
+    if heads:
+        over.update(scale_per_head=True, head_gain=(0.5, 2.0, 1.0, 4.0))
+    case = workloads.make_case(workloads.small_spec(cfg, **over))
+    kc, vc = oracle_caches(case)
+    units = [(b, h) for b in range(case.B) for h in range(case.spec.num_kv_heads)][::3]
+    uk, uv = unit_caches(case, units, head_tables(case))
+    P = case.spec.page_size
+    for b, h in units:
+        n = int(case.seq_lens[b])
+        pages = case.block_table[b, :-(-n // P)]
+        a = kc[pages, h].reshape(-1, case.spec.head_dim)[:n]
+        assert np.array_equal(uk[pages, h].reshape(-1, case.spec.head_dim)[:n], a)
+        assert np.array_equal(uv[pages, h].reshape(-1, case.spec.head_dim)[:n],
+                              vc[pages, h].reshape(-1, case.spec.head_dim)[:n])

@@ -5,9 +5,10 @@ engine whose memory pool already holds nearly all device memory, or a
 serving loop where an allocation's implicit device synchronisation is not
 acceptable. Its split scratch is a fixed array inside the library. This file
 is collected last on purpose: it checks the new entry point through the C
-ABI against the ordinary one (which takes a caller workspace), on two calls
-in a row, and passes both alone in a fresh process and after every other
-test.
+ABI against the ordinary one (which takes a caller workspace) and against
+the oracle, on two calls in a row, and passes both alone in a fresh process
+and after every other test. Every case is one whose plan splits the keys,
+so the built-in array is really used.
 """
 
 import pytest
@@ -15,7 +16,8 @@ import torch
 
 from paged_fp8_kv_cache_gb300 import binding as pf
 from paged_fp8_kv_cache_gb300 import workloads
-from tests.gpu_helpers import GpuCase
+from tests.gpu_helpers import GpuCase, assert_close
+from tests.oracle_helpers import oracle_attention, oracle_caches
 
 pytestmark = pytest.mark.gpu
 
@@ -35,15 +37,22 @@ def _static_decode(g, num_splits):
 
 @pytest.mark.parametrize("spec,splits", [
     (workloads.small_spec(3, contexts=(5000,)), 7),                      # long E4M3 decode, split
-    (workloads.small_spec(4, contexts=(4100, 2500)), 0),                 # q8 verify, automatic plan
+    (workloads.small_spec(4, contexts=(4100, 2500)), 4),                 # q8 verify on tcgen05, split
     (workloads.small_spec(5, contexts=("loguniform", 30, 700, 64)), 3),  # ragged batch
 ], ids=["long-e4m3", "verify-q8-e5m2", "mixed-e4m3"])
 def test_static_scratch_matches_workspace_entry_point(pflib, spec, splits):
     pf.pfkv_device_errors(clear=True)
     case = workloads.make_case(spec)
+    s = case.spec
+    # the plan splits the keys, so the partials go through the built-in array
+    need = pf.pfkv_decode_workspace_bytes(case.B, s.num_q_tokens, s.num_q_heads, s.num_kv_heads, s.head_dim,
+                                          s.page_size, s.kv_dtype, int(case.seq_lens.max()), splits)
+    assert need > 0
     g = GpuCase(case)
     ref_out, ref_lse = g.decode(num_splits=splits)
     torch.cuda.synchronize()
+    kc, vc = oracle_caches(case)
+    o_oracle, l_oracle = oracle_attention(case, kc, vc)
     for _ in range(2):  # two calls in a row share (and reuse) the built-in array
         out, lse = _static_decode(g, splits)
         torch.cuda.synchronize()
@@ -52,6 +61,7 @@ def test_static_scratch_matches_workspace_entry_point(pflib, spec, splits):
         fin = torch.isfinite(ref_lse)
         assert torch.equal(fin, torch.isfinite(lse))
         assert (lse[fin] - ref_lse[fin]).abs().max().item() <= LSE_TOL
+        assert_close(out, lse, o_oracle, l_oracle, out_tol=OUT_TOL, lse_tol=LSE_TOL)
     assert pf.pfkv_device_errors(clear=True) == 0
 
 
