@@ -100,6 +100,12 @@ typedef enum {
 #define PFKV_CAP_Q_TOKENS_1_16  0x4000u /* 1..16 causal query tokens (a q16 verify), rows <= 64 */
 #define PFKV_CAP_SPLIT_KV       0x2000u /* split-KV partitions + LSE merge kernel */
 #define PFKV_CAP_SCALES_PER_HEAD 0x8000u /* PFKV_KV_SCALES_PER_HEAD: one FP8 scale per KV head */
+#define PFKV_CAP_NON_CAUSAL     0x10000u /* pfkv_paged_attention without PFKV_MASK_CAUSAL */
+#define PFKV_CAP_SLIDING_WINDOW 0x20000u /* pfkv_paged_attention with window > 0 (prefix tiles skipped) */
+#define PFKV_CAP_PREFILL        0x40000u /* pfkv_paged_attention with up to 8192 query tokens per sequence */
+
+/* The mask argument of pfkv_paged_attention (a bit set). */
+#define PFKV_MASK_CAUSAL 0x1  /* query t sees no key after its own position */
 
 /*
  * pfkv_kv_cache_append -- quantise new K/V tokens and write them into their
@@ -247,6 +253,57 @@ PFKV_API pfkv_status pfkv_paged_attention_decode(void* out, float* lse, const vo
                                         int max_seq_len, int num_splits,
                                         void* workspace, size_t workspace_bytes,
                                         pfkv_stream_t stream);
+
+/*
+ * pfkv_paged_attention -- the same paged attention with a choice of mask and
+ * any number of query tokens per sequence: the non-causal sliding-window
+ * draft attention ([R2] "Production DFlash2 on V100": non-causal
+ * sliding-window draft attention; [R2] "Flash-V100 long-context
+ * improvements": the draft's sliding-window attention skips the prefix tiles
+ * it does not use) and the chunked prefill over the paged FP8 cache ([R2]
+ * "Flash-V100 long-context improvements": the long-prefill GQA path that
+ * packs the heads of a group into wider tensor-core work; [R3] the prefill
+ * chunk budgets of the profile).
+ *
+ * Arguments, layouts and results as pfkv_paged_attention_decode, plus:
+ *   mask    PFKV_MASK_CAUSAL, or 0 for a non-causal block of queries
+ *   window  0 (none), or W > 0: query t sees no key W or more positions
+ *           before its own
+ * For query t at position p = N - T + t the visible keys are lo <= j <= hi
+ * with hi = p (causal) or N - 1 (not), lo = max(0, p - W + 1) (window) or 0.
+ * (A reading: the pages name the mask but do not define it; the window
+ * bounds how far back a query looks, the causal bit how far forward.) Keys
+ * wholly before every query's window are never read, so the cost of a
+ * windowed call does not grow with the context.
+ * Supported: 1 <= num_q_tokens <= 8192 and a group of at most 64 query heads
+ * per KV head; the T tokens are processed in slabs of up to 64 rows (tokens x
+ * heads of the group) per CTA. num_splits, the workspace and its layout are
+ * as for the decode, sized by pfkv_attention_plan /
+ * pfkv_attention_workspace_bytes (same arguments plus mask and window); a
+ * row's split partials cover the ranges of its slab only.
+ */
+PFKV_API pfkv_status pfkv_paged_attention(void* out, float* lse, const void* q,
+                                 const void* k_cache, const void* v_cache,
+                                 const int32_t* block_table, int max_blocks_per_seq,
+                                 const int32_t* seq_lens, int num_seqs, int num_q_tokens,
+                                 int num_q_heads, int num_kv_heads, int head_dim,
+                                 int page_size, int num_blocks, pfkv_kv_dtype dtype,
+                                 const float* k_scale, const float* v_scale,
+                                 float softmax_scale, int mask, int window,
+                                 int max_seq_len, int num_splits, void* workspace,
+                                 size_t workspace_bytes, pfkv_stream_t stream);
+
+/* pfkv_attention_plan / pfkv_attention_workspace_bytes -- pfkv_decode_plan and
+ * pfkv_decode_workspace_bytes for pfkv_paged_attention (same meaning; the
+ * mask and window change the key span a CTA covers). */
+PFKV_API pfkv_status pfkv_attention_plan(int num_seqs, int num_q_tokens, int num_q_heads,
+                                int num_kv_heads, int head_dim, int page_size,
+                                pfkv_kv_dtype dtype, int mask, int window, int max_seq_len,
+                                int num_splits_request, int* num_splits, int* split_tokens);
+PFKV_API size_t pfkv_attention_workspace_bytes(int num_seqs, int num_q_tokens, int num_q_heads,
+                                      int num_kv_heads, int head_dim, int page_size,
+                                      pfkv_kv_dtype dtype, int mask, int window,
+                                      int max_seq_len, int num_splits_request);
 
 /*
  * pfkv_paged_attention_decode_static_scratch -- pfkv_paged_attention_decode

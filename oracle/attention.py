@@ -15,9 +15,18 @@ definition, computed in float64:
 for sequence b, query token t < T and query head h:
 
 * ``kvh = h // g`` with ``g = Hq // Hkv`` (contiguous head groups);
-* query t sits at position ``N_b - T + t`` (``seq_lens[b] = N_b`` already
-  counts the T query tokens, whose K/V are in the cache) and sees keys
-  ``j = 0 .. N_b - T + t`` (causal over its own drafts);
+* query t sits at position ``p = N_b - T + t`` (``seq_lens[b] = N_b``
+  already counts the T query tokens, whose K/V are in the cache) and sees
+  the keys ``lo <= j <= hi`` with
+  ``hi = p`` when causal (over its own drafts, the default) or ``hi = N_b - 1``
+  when not (a draft block attending to all of its own tokens: the non-causal
+  draft attention of "1Cat-vLLM 1.5.0", "Production DFlash2 on V100"), and
+  ``lo = max(0, p - W + 1)`` for a sliding window of W keys (the draft's
+  sliding-window attention, same page, "Flash-V100 long-context
+  improvements") or ``lo = 0`` without one (W = 0). A window is read as a
+  bound on how far back a query looks, relative to its own position; the
+  causal flag alone bounds how far forward. Long T is the chunked prefill
+  (the same attention for every token of a prompt chunk);
 * key j lives at ``page = block_table[b][j // P]``, ``offset = j % P``;
 * ``k_j = decode(K[page, kvh, offset]) * k_scale`` and likewise ``v_j``
   (``k_scale`` is the pool's static scale, or KV head kvh's when one scale
@@ -28,8 +37,9 @@ for sequence b, query token t < T and query head h:
 * ``out = sum_j w_j v_j / L`` and ``lse = m + ln L`` (natural log, the logits
   include both ``softmax_scale`` and ``k_scale``).
 
-A row that sees no key (``N_b - T + t < 0``, e.g. an empty sequence) has
-``out = 0`` and ``lse = -inf`` (the empty-sum convention used on both sides).
+A row that sees no key (e.g. ``N_b - T + t < 0`` when causal, or an empty
+sequence) has ``out = 0`` and ``lse = -inf`` (the empty-sum convention used
+on both sides).
 
 Evaluation order: per (sequence, KV head) all logits of all rows over the
 whole key range are formed first, then the weights, then ``sum_j w_j v_j``.
@@ -57,7 +67,8 @@ def paged_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
                     block_table: np.ndarray, seq_lens: np.ndarray,
                     num_q_tokens: int, num_kv_heads: int, page_size: int,
                     kv_dtype: str, k_scale: float, v_scale: float,
-                    softmax_scale: float, units=None, token_range=None):
+                    softmax_scale: float, units=None, token_range=None, causal=True, window=0,
+                    tokens=None):
     """Attention for every (or the listed) (sequence, KV head) unit.
 
     q: fp16 ``[B*T, Hq, D]``. Caches ``[num_blocks, Hkv, P, D]`` (uint8 codes or
@@ -65,8 +76,12 @@ def paged_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
     units not listed in ``units`` are left NaN.
 
     ``token_range=(lo, hi)`` restricts every row to keys ``lo <= j < hi`` (on
-    top of its causal limit). It is how the split-KV partial results are
-    defined: the attention of a row over one contiguous range of its keys.
+    top of its mask). It is how the split-KV partial results are defined: the
+    attention of a row over one contiguous range of its keys.
+
+    ``causal`` and ``window`` (W >= 0; 0 = no window) set each row's visible
+    keys as stated at the top of this module. ``tokens`` (a list of query
+    token indices) computes only those tokens' rows (the others stay NaN).
     """
     T = num_q_tokens
     q = np.asarray(q)
@@ -89,14 +104,19 @@ def paged_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
         vs = vs_all[kvh if vs_all.size > 1 else 0]
         n = int(seq_lens[b])
         heads = list(range(kvh * g, (kvh + 1) * g))
+        toks = list(range(T)) if tokens is None else [int(t) for t in tokens]
+        nt = len(toks)
         # rows of this unit: (t, head) -> q vector
-        qrows = q[b * T:(b + 1) * T, heads, :].astype(np.float64)  # [T, g, D]
-        qrows = qrows.reshape(T * g, D)
-        last = np.array([n - T + t for t in range(T) for _ in heads])  # per row
+        qrows = q[b * T:(b + 1) * T, heads, :].astype(np.float64)[toks]  # [nt, g, D]
+        qrows = qrows.reshape(nt * g, D)
+        # per row: the first and last visible key
+        pos = np.array([n - T + t for t in toks for _ in heads])
+        last = pos if causal else np.full(nt * g, n - 1)
+        first = np.maximum(0, pos - window + 1) if window > 0 else np.zeros(nt * g, dtype=np.int64)
         lo, hi = (0, n) if token_range is None else (max(0, token_range[0]), min(n, token_range[1]))
         if hi <= lo:
-            o = np.zeros((T * g, D))
-            l_ = np.full(T * g, -np.inf)
+            o = np.zeros((nt * g, D))
+            l_ = np.full(nt * g, -np.inf)
         else:
             first_page, last_page = lo // page_size, (hi - 1) // page_size
             pages = np.asarray(block_table[b, first_page:last_page + 1], dtype=np.int64)
@@ -105,7 +125,7 @@ def paged_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
             K = _decode_pages(k_cache, pages, kvh, kv_dtype)[lo - base:hi - base] * ks
             s = sm * (qrows @ K.T)  # [rows, hi-lo]
             j = np.arange(lo, hi)
-            visible = j[None, :] <= last[:, None]
+            visible = (j[None, :] <= last[:, None]) & (j[None, :] >= first[:, None])
             s = np.where(visible, s, -np.inf)
             m = s.max(axis=1)
             has = np.isfinite(m)
@@ -117,9 +137,9 @@ def paged_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
             acc = w @ V
             o = np.where(has[:, None], acc / np.where(has, L, 1.0)[:, None], 0.0)
             l_ = np.where(has, m + np.log(np.where(has, L, 1.0)), -np.inf)
-        o = o.reshape(T, g, D)
-        l_ = l_.reshape(T, g)
-        for t in range(T):
-            out[b * T + t, heads, :] = o[t]
-            lse[b * T + t, heads] = l_[t]
+        o = o.reshape(nt, g, D)
+        l_ = l_.reshape(nt, g)
+        for i, t in enumerate(toks):
+            out[b * T + t, heads, :] = o[i]
+            lse[b * T + t, heads] = l_[i]
     return out, lse

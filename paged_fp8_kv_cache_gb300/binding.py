@@ -33,6 +33,7 @@ PFKV_DEVERR_BLOCK_ID = 0x2
 PFKV_DEVERR_SEQ_LEN = 0x4
 PFKV_DEVERR_TIMEOUT = 0x8
 PFKV_KV_SCALES_PER_HEAD = 0x100  # OR into an FP8 dtype: one scale per KV head
+PFKV_MASK_CAUSAL = 0x1
 
 # every entry point declared in include/pfkv.h
 EXPORTS = [
@@ -41,6 +42,9 @@ EXPORTS = [
     "pfkv_decode_plan",
     "pfkv_decode_workspace_bytes",
     "pfkv_paged_attention_decode",
+    "pfkv_paged_attention",
+    "pfkv_attention_plan",
+    "pfkv_attention_workspace_bytes",
     "pfkv_paged_attention_decode_static_scratch",
     "pfkv_lse_merge",
     "pfkv_device_errors",
@@ -86,6 +90,13 @@ def load(path: str | None = None):
     lib.pfkv_paged_attention_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32,
                                                 i32, vp, vp, ctypes.c_float, i32, i32, vp, ctypes.c_size_t, vp]
     lib.pfkv_paged_attention_decode.restype = i32
+    lib.pfkv_paged_attention.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32,
+                                         i32, vp, vp, ctypes.c_float, i32, i32, i32, i32, vp, ctypes.c_size_t, vp]
+    lib.pfkv_paged_attention.restype = i32
+    lib.pfkv_attention_plan.argtypes = [i32] * 11 + [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+    lib.pfkv_attention_plan.restype = i32
+    lib.pfkv_attention_workspace_bytes.argtypes = [i32] * 11
+    lib.pfkv_attention_workspace_bytes.restype = ctypes.c_size_t
     lib.pfkv_paged_attention_decode_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
                                                                i32, i32, i32, i32, vp, vp, ctypes.c_float, i32,
                                                                i32, vp]
@@ -184,6 +195,44 @@ def pfkv_paged_attention_decode(out, lse, q, k_cache, v_cache, block_table, seq_
         _kv_scaled(kv_dtype, k_scale, v_scale, num_kv_heads), _ptr(k_scale), _ptr(v_scale), float(softmax_scale),
         max_seq_len, num_splits, _ptr(workspace), ws_bytes,
         _stream(stream)))
+
+
+def _mask(causal) -> int:
+    return PFKV_MASK_CAUSAL if causal else 0
+
+
+def pfkv_attention_plan(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, kv_dtype,
+                        max_seq_len, causal=True, window=0, num_splits_request=0):
+    lib = load()
+    ns, st = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib.pfkv_attention_plan(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size,
+                                   _kv(kv_dtype), _mask(causal), window, max_seq_len, num_splits_request,
+                                   ctypes.byref(ns), ctypes.byref(st)))
+    return ns.value, st.value
+
+
+def pfkv_attention_workspace_bytes(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, kv_dtype,
+                                   max_seq_len, causal=True, window=0, num_splits_request=0) -> int:
+    lib = load()
+    return int(lib.pfkv_attention_workspace_bytes(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim,
+                                                  page_size, _kv(kv_dtype), _mask(causal), window, max_seq_len,
+                                                  num_splits_request))
+
+
+def pfkv_paged_attention(out, lse, q, k_cache, v_cache, block_table, seq_lens, num_q_tokens, num_kv_heads, page_size,
+                         kv_dtype, k_scale, v_scale, softmax_scale, max_seq_len, causal=True, window=0, num_splits=0,
+                         workspace=None, stream=None):
+    """Paged attention with a mask choice (causal or not, sliding window of ``window`` keys, 0 = none) and up to
+    8192 query tokens per sequence (chunked prefill); tensors as pfkv_paged_attention_decode."""
+    lib = load()
+    num_seqs = seq_lens.shape[0]
+    hq, d = q.shape[1], q.shape[2]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.pfkv_paged_attention(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), num_seqs, num_q_tokens, hq, num_kv_heads, d, page_size, k_cache.shape[0],
+        _kv_scaled(kv_dtype, k_scale, v_scale, num_kv_heads), _ptr(k_scale), _ptr(v_scale), float(softmax_scale),
+        _mask(causal), window, max_seq_len, num_splits, _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def pfkv_paged_attention_decode_static_scratch(out, lse, q, k_cache, v_cache, block_table, seq_lens, num_q_tokens,

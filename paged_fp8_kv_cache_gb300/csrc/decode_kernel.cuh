@@ -1,11 +1,15 @@
 // Paged decode / grouped causal-verify attention over an FP8 (or fp16)
 // KV cache: the split-KV partial kernel.
 //
-// One CTA handles one (key range, KV head, sequence). Its rows are the
-// T * g query rows (query token t, head of the group) that share the KV
-// head -- one tile for ordinary GQA decode and for the grouped q8 verifier
-// ("1Cat-vLLM 1.5.0", "Flash-V100 long-context improvements": grouped q8
-// verifier, page-ID reuse, 128-bit cache loads, long-context split route).
+// One CTA handles one (key range, KV head, query slab, sequence). Its rows
+// are the query rows (query token t of the slab, head of the group) that
+// share the KV head -- all T * g rows for ordinary GQA decode and for the
+// grouped q8 verifier ("1Cat-vLLM 1.5.0", "Flash-V100 long-context
+// improvements": grouped q8 verifier, page-ID reuse, 128-bit cache loads,
+// long-context split route), up to 64 rows of a prefill chunk's slab. The
+// mask (causal or not, sliding window) bounds each row's keys from both
+// sides; a CTA's key range starts at its slab's lowest visible key, so the
+// tiles before a window are never read (mask_span.h).
 //
 // Warp roles:
 //  * one producer warp: walks the key range 64 keys at a time, reads each
@@ -33,6 +37,7 @@
 
 #include "device_utils.cuh"
 #include "frag_layout.h"
+#include "mask_span.h"
 #include "pfkv_internal.h"
 
 namespace pfkv {
@@ -72,21 +77,22 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
   // derived from it stays a shared-memory pointer (32-bit shared loads and stores)
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int split = blockIdx.x, b = blockIdx.z;
+  const int kvh = blockIdx.y % p.num_kv_heads;
+  const int slab = p.num_slabs - 1 - static_cast<int>(blockIdx.y) / p.num_kv_heads;  // longest slabs first
   const int ncw = p.nrg * p.nts;
-  const int R = p.T * p.G;
 
   // launched with programmatic stream serialisation: wait for the preceding
   // grid (which may produce q, the cache or the tables) before any global read
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // The producer warp fetches the block-table entries of the range's first 32 pages now, so
-  // that the load overlaps the sequence-length load (the range's first page does not depend
-  // on the length; entries stay inside the table row; they are validated once the length is
-  // known).
-  const int pfirst0 = (split * p.split_tokens) >> p.page_shift;
+  // Without a window the range's first page does not depend on the sequence length: the
+  // producer warp fetches the block-table entries of its first 32 pages now, so that the load
+  // overlaps the sequence-length load (entries stay inside the table row; they are validated
+  // once the length is known). With a window the fetch waits for the length.
+  const int pguess = p.window > 0 ? -1 : (split * p.split_tokens) >> p.page_shift;
   int pre_id = 0;
-  if ((threadIdx.x >> 5) == ncw) {
-    const int m = pfirst0 + (threadIdx.x & 31);
+  if ((threadIdx.x >> 5) == ncw && pguess >= 0) {
+    const int m = pguess + (threadIdx.x & 31);
     if (m < p.max_blocks) pre_id = p.block_table[static_cast<size_t>(b) * p.max_blocks + m];
   }
   // sequence length, validated against what the block table can address
@@ -94,15 +100,18 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
   {
     const int cap = min(p.max_seq_len, p.max_blocks * p.page_size);
     if (N < 0 || N > cap) {
-      if (threadIdx.x == 0 && split == 0 && kvh == 0) atomicOr(p.err, kDevErrSeqLen);
+      if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) atomicOr(p.err, kDevErrSeqLen);
       N = N < 0 ? 0 : cap;
     }
   }
-  const int nsplit_b = N > 0 ? (N + p.split_tokens - 1) / p.split_tokens : 1;
+  const SlabSpan sp = slab_span(N, p.T, slab, p.slab_tokens, p.causal, p.window, kTileKeys);
+  const int nsplit_b = span_splits(sp, p.split_tokens);
   if (split >= nsplit_b) return;
-  const int t0 = split * p.split_tokens;
-  const int t1 = min(N, t0 + p.split_tokens);
+  const int R = (sp.ts1 - sp.ts0) * p.G;  // query rows of this slab
+  const int t0 = sp.base + split * p.split_tokens;
+  const int t1 = sp.hi >= sp.lo ? min(sp.hi + 1, t0 + p.split_tokens) : t0;
   const int ntiles = t1 > t0 ? (t1 - t0 + kTileKeys - 1) / kTileKeys : 0;
+  const int pfirst0 = t0 >> p.page_shift;
 
   const int body_bytes = decode_smem_bytes<D, KV, NT>(ncw) - ncw * ROWS_W * 8 - 2 * NS * 8;
   float2* ml_buf = reinterpret_cast<float2*>(smem + body_bytes);  // [ncw][ROWS_W] (m, l)
@@ -138,7 +147,7 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
       {
         const int mine = chunk_base + lane;
         if (mine <= page_last) {
-          my_id = pre_id;
+          my_id = pguess == pfirst0 ? pre_id : bt[mine];
           if (static_cast<unsigned>(my_id) >= static_cast<unsigned>(p.num_blocks)) {
             atomicOr(p.err, kDevErrBlockId);
             my_id = 0;
@@ -243,8 +252,8 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
     const int row = row_base + nt * 8 + g8;
     const __half* qrow = nullptr;
     if (row < R) {
-      const int t = row / p.G, j = row - t * p.G;
-      qrow = p.q + ((static_cast<size_t>(b) * p.T + t) * p.num_q_heads + kvh * p.G + j) * D;
+      const int tl = row / p.G, j = row - tl * p.G;
+      qrow = p.q + ((static_cast<size_t>(b) * p.T + sp.ts0 + tl) * p.num_q_heads + kvh * p.G + j) * D;
     }
 #pragma unroll
     for (int ks = 0; ks < KSTEPS; ++ks) {
@@ -258,20 +267,27 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
     }
   }
 
-  // causal limit of the two rows (2c, 2c+1) of every n-tile this lane accumulates
-  int lim[NT][2];
-  int min_lim = INT_MAX;
+  // query token of the two rows (2c, 2c+1) of every n-tile this lane accumulates; the rows'
+  // visible keys [key_lo, key_hi] follow from it where a group needs masking (padding rows past
+  // R take the slab's last token: they are never written out)
+  int rtok[NT][2];
+  int min_hi = INT_MAX, max_lo = 0;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int row = row_base + nt * 8 + 2 * c + e;
-      const int t = row / p.G;  // rows past R get t >= T: limited by N only
-      lim[nt][e] = min(N - 1, N - p.T + t);
-      if (row < R) min_lim = min(min_lim, lim[nt][e]);
+      rtok[nt][e] = row < R ? sp.ts0 + row / p.G : sp.ts1 - 1;
+      if (row < R) {
+        min_hi = min(min_hi, key_hi(N, p.T, rtok[nt][e], p.causal));
+        max_lo = max(max_lo, key_lo(N, p.T, rtok[nt][e], p.window));
+      }
     }
 #pragma unroll
-  for (int off = 1; off < 4; off <<= 1) min_lim = min(min_lim, __shfl_xor_sync(0xffffffffu, min_lim, off));
+  for (int off = 1; off < 4; off <<= 1) {
+    min_hi = min(min_hi, __shfl_xor_sync(0xffffffffu, min_hi, off));
+    max_lo = max(max_lo, __shfl_xor_sync(0xffffffffu, max_lo, off));
+  }
 
   float o[MTILES][NT][4];
 #pragma unroll
@@ -370,7 +386,7 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
         }
 
       // ---- scale, mask, running max
-      const bool need_mask = (key0 + 15 > min_lim);
+      const bool need_mask = (key0 + 15 > min_hi) || (key0 < max_lo);
       const int keyA = key0 + g8, keyB = keyA + 8;
       float mx[NT][2];
 #pragma unroll
@@ -379,8 +395,10 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
         for (int e = 0; e < 2; ++e) {
           float sa = sacc[nt][e] * sc2, sb = sacc[nt][2 + e] * sc2;
           if (need_mask) {
-            if (keyA > lim[nt][e]) sa = -CUDART_INF_F;
-            if (keyB > lim[nt][e]) sb = -CUDART_INF_F;
+            const int khi = key_hi(N, p.T, rtok[nt][e], p.causal);
+            const int klo = key_lo(N, p.T, rtok[nt][e], p.window);
+            if (keyA > khi || keyA < klo) sa = -CUDART_INF_F;
+            if (keyB > khi || keyB < klo) sb = -CUDART_INF_F;
           }
           sacc[nt][e] = sa;
           sacc[nt][2 + e] = sb;
@@ -572,8 +590,8 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
       }
       const bool has = (M != -CUDART_INF_F) && (L > 0.f);
       const float inv = has ? vscale / L : 0.f;
-      const int t = r / p.G, j = r - t * p.G;
-      const size_t grow = (static_cast<size_t>(b) * p.T + t) * p.num_q_heads + kvh * p.G + j;
+      const int tl = r / p.G, j = r - tl * p.G;
+      const size_t grow = (static_cast<size_t>(b) * p.T + sp.ts0 + tl) * p.num_q_heads + kvh * p.G + j;
       // natural-log LSE from base-2 running values
       const float lse_val = has ? (M + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
       if (final_out) {
@@ -615,8 +633,8 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
     const bool has = (M != -CUDART_INF_F) && (L > 0.f);
     const float inv = has ? vscale / L : 0.f;
     s_coef[r] = make_float4(w[0] * inv, w[1] * inv, w[2] * inv, w[3] * inv);
-    const int t = r / p.G, j = r - t * p.G;
-    const long long grow = (static_cast<long long>(b) * p.T + t) * p.num_q_heads + kvh * p.G + j;
+    const int tl = r / p.G, j = r - tl * p.G;
+    const long long grow = (static_cast<long long>(b) * p.T + sp.ts0 + tl) * p.num_q_heads + kvh * p.G + j;
     const float lse_val = has ? (M + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
     if (final_out) {
       s_orow[r] = grow * D;

@@ -14,6 +14,7 @@
 
 #include "../../include/pfkv.h"
 #include "frag_layout.h"
+#include "mask_span.h"
 #include "pfkv_internal.h"
 
 namespace pfkv {
@@ -194,6 +195,9 @@ int log2i(int x) {
   return s;
 }
 
+constexpr int kMaxQTokens = 8192;  // query tokens per sequence of one call (a prefill chunk)
+constexpr int kMaxRows = 64;       // query rows per CTA (a slab of tokens x the group's heads)
+
 struct Plan {
   DecodeLaunch cfg;
   int nrg, nts, ncw;  // mma.sync decode kernel: row groups x key slices of consumer warps
@@ -201,6 +205,8 @@ struct Plan {
   int nmax;           // its padded row count (32, 48, 64)
   int tile;           // keys per pipeline tile (split ranges are multiples of it)
   int splits, split_tokens;
+  int causal, window;          // the mask (window 0 when it cannot bind: at least max_seq_len)
+  int slab_tokens, num_slabs;  // query tokens per CTA
 };
 
 int ctas_per_sm(int dev, const DecodeLaunch& cfg, int ncw, bool tc, int nmax) {
@@ -231,28 +237,40 @@ int ctas_per_sm(int dev, const DecodeLaunch& cfg, int ncw, bool tc, int nmax) {
   return n;
 }
 
-// Shape checks shared by plan / workspace / decode.
-pfkv_status check_shape(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_kv_dtype dtype, int max_seq_len,
-                        int num_splits) {
-  if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || max_seq_len < 0 || num_splits < 0)
-    return fail(PFKV_ERR_INVALID_ARG, "negative size (num_seqs=%d Hq=%d Hkv=%d max_seq_len=%d num_splits=%d)",
-                num_seqs, Hq, Hkv, max_seq_len, num_splits);
+// Shape checks shared by plan / workspace / attention.
+pfkv_status check_shape(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_kv_dtype dtype, int mask,
+                        int window, int max_seq_len, int num_splits) {
+  if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || max_seq_len < 0 || num_splits < 0 || window < 0)
+    return fail(PFKV_ERR_INVALID_ARG,
+                "negative size (num_seqs=%d Hq=%d Hkv=%d max_seq_len=%d num_splits=%d window=%d)", num_seqs, Hq,
+                Hkv, max_seq_len, num_splits, window);
   if (Hq % Hkv != 0) return fail(PFKV_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d", Hq, Hkv);
   if (!valid_dtype(dtype)) return fail(PFKV_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(dtype));
-  if (T < 1 || T > 16) return fail(PFKV_ERR_UNSUPPORTED, "num_q_tokens %d outside 1..16", T);
+  if (mask & ~PFKV_MASK_CAUSAL) return fail(PFKV_ERR_INVALID_ARG, "unknown mask bits 0x%x", mask);
+  if (T < 1 || T > kMaxQTokens) return fail(PFKV_ERR_UNSUPPORTED, "num_q_tokens %d outside 1..%d", T, kMaxQTokens);
   if (D != 128 && D != 256) return fail(PFKV_ERR_UNSUPPORTED, "head_dim %d (supported: 128, 256)", D);
   if (!is_pow2(P) || P < 16 || P > 2048)
     return fail(PFKV_ERR_UNSUPPORTED, "page_size %d (supported: powers of two 16..2048)", P);
-  if (T * (Hq / Hkv) > 64)
-    return fail(PFKV_ERR_UNSUPPORTED, "num_q_tokens * group size = %d > 64 rows per KV head", T * (Hq / Hkv));
+  if (Hq / Hkv > kMaxRows) return fail(PFKV_ERR_UNSUPPORTED, "group size %d > %d", Hq / Hkv, kMaxRows);
+  if (static_cast<long long>(num_seqs) * T * Hq > 0x7fffffffLL)
+    return fail(PFKV_ERR_UNSUPPORTED, "num_seqs * num_q_tokens * num_q_heads exceeds 2^31");
   return PFKV_OK;
 }
 
-pfkv_status make_plan(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_kv_dtype dtype, int max_seq_len,
-                      int num_splits_request, Plan* pl) {
-  pfkv_status st = check_shape(num_seqs, T, Hq, Hkv, D, P, dtype, max_seq_len, num_splits_request);
+pfkv_status make_plan(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_kv_dtype dtype, int mask, int window,
+                      int max_seq_len, int num_splits_request, Plan* pl) {
+  pfkv_status st = check_shape(num_seqs, T, Hq, Hkv, D, P, dtype, mask, window, max_seq_len, num_splits_request);
   if (st != PFKV_OK) return st;
-  const int R = T * (Hq / Hkv);
+  const int G = Hq / Hkv;
+  // query slabs: every token in one CTA when its rows fit, else slabs of 64 / G tokens
+  pl->slab_tokens = T * G <= kMaxRows ? T : kMaxRows / G;
+  pl->num_slabs = (T + pl->slab_tokens - 1) / pl->slab_tokens;
+  if (static_cast<long long>(Hkv) * pl->num_slabs > 65535)
+    return fail(PFKV_ERR_UNSUPPORTED, "num_kv_heads * query slabs = %lld > 65535",
+                static_cast<long long>(Hkv) * pl->num_slabs);
+  pl->causal = (mask & PFKV_MASK_CAUSAL) ? 1 : 0;
+  pl->window = window >= max_seq_len ? 0 : window;  // a window of at least every length never binds
+  const int R = pl->slab_tokens * G;
   pl->cfg.head_dim = D;
   pl->cfg.kv = kv_of(dtype);
   pl->cfg.nt = R <= 8 ? 1 : 2;
@@ -263,7 +281,14 @@ pfkv_status make_plan(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_k
   pl->tc = (dtype != PFKV_KV_FP16) && R > 16;
   pl->nmax = R <= 32 ? 32 : (R <= 48 ? 48 : 64);
   pl->tile = pl->tc ? 128 : kTileKeys;
-  const int tiles = max_seq_len > 0 ? (max_seq_len + pl->tile - 1) / pl->tile : 1;
+  // the longest key span of a slab: the sequence, or with a window the window plus the tokens
+  // a slab's rows spread over (all T without the causal bound) plus the tile alignment
+  long long span = max_seq_len;
+  if (pl->window > 0) {
+    const long long w = static_cast<long long>(pl->causal ? pl->slab_tokens : T) + pl->window + pl->tile;
+    if (w < span) span = w;
+  }
+  const int tiles = span > 0 ? static_cast<int>((span + pl->tile - 1) / pl->tile) : 1;
   int want;
   if (num_splits_request > 0) {
     want = num_splits_request;
@@ -272,7 +297,7 @@ pfkv_status make_plan(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_k
     cudaError_t e = current_device(&dev);
     if (e == cudaSuccess) e = sm_count(dev, &sms);
     if (e != cudaSuccess) return cuda_fail(e, "device query");
-    const int units = num_seqs > 0 ? num_seqs * Hkv : 1;
+    const int units = num_seqs > 0 ? num_seqs * Hkv * pl->num_slabs : 1;
     const int occ = ctas_per_sm(dev, pl->cfg, pl->ncw, pl->tc, pl->nmax);
     int base = (sms * occ + units - 1) / units;
     // Long ranges at full occupancy: one CTA per SM with ranges twice as long measured faster
@@ -286,7 +311,7 @@ pfkv_status make_plan(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_k
     // SM, with a fixed start-up and first-tile cost worth ~8 tiles: two waves of half-length
     // ranges cost more than one wave).
     const int max_keys = (pl->tc ? 2 : 1) * (R * 256 > 2048 ? R * 256 : 2048);
-    const int need = (long_ranges && units < sms) ? 1 : (max_seq_len + max_keys - 1) / max_keys;
+    const int need = (long_ranges && units < sms) ? 1 : static_cast<int>((span + max_keys - 1) / max_keys);
     const int k = base > 0 ? (need + base - 1) / base : 1;
     want = base * (k > 1 ? k : 1);
   }
@@ -304,6 +329,155 @@ size_t workspace_for(const Plan& pl, int num_seqs, int T, int Hq, int D) {
   const size_t o = rows * pl.splits * D * sizeof(float);
   const size_t l = rows * pl.splits * sizeof(float);
   return o + l;
+}
+
+// The decode entry points keep their contract: causal, no window, 1..16 query tokens whose rows
+// (tokens x group heads) fit one CTA.
+pfkv_status check_decode_tokens(int T, int Hq, int Hkv) {
+  if (T < 1 || T > 16) return fail(PFKV_ERR_UNSUPPORTED, "num_q_tokens %d outside 1..16", T);
+  if (Hkv > 0 && Hq % Hkv == 0 && T * (Hq / Hkv) > kMaxRows)
+    return fail(PFKV_ERR_UNSUPPORTED, "num_q_tokens * group size = %d > %d rows per KV head", T * (Hq / Hkv),
+                kMaxRows);
+  return PFKV_OK;
+}
+
+pfkv_status plan_impl(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                      pfkv_kv_dtype dtype_arg, int mask, int window, int max_seq_len, int num_splits_request,
+                      int* num_splits, int* split_tokens) {
+  pfkv_kv_dtype dtype;
+  int unused_stride;
+  if (!split_dtype(dtype_arg, &dtype, &unused_stride))
+    return fail(PFKV_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(dtype_arg));
+  Plan pl;
+  pfkv_status st = make_plan(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype, mask,
+                             window, max_seq_len, num_splits_request, &pl);
+  if (st != PFKV_OK) return st;
+  if (num_splits) *num_splits = pl.splits;
+  if (split_tokens) *split_tokens = pl.split_tokens;
+  return PFKV_OK;
+}
+
+size_t workspace_impl(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                      pfkv_kv_dtype dtype_arg, int mask, int window, int max_seq_len, int num_splits_request) {
+  pfkv_kv_dtype dtype;
+  int unused_stride;
+  if (!split_dtype(dtype_arg, &dtype, &unused_stride)) return 0;
+  Plan pl;
+  if (make_plan(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype, mask, window,
+                max_seq_len, num_splits_request, &pl) != PFKV_OK)
+    return 0;
+  return workspace_for(pl, num_seqs, num_q_tokens, num_q_heads, head_dim);
+}
+
+pfkv_status attention_impl(void* out, float* lse, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                           int num_q_tokens, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                           int num_blocks, pfkv_kv_dtype dtype_arg, const float* k_scale, const float* v_scale,
+                           float softmax_scale, int mask, int window, int max_seq_len, int num_splits,
+                           void* workspace, size_t workspace_bytes, pfkv_stream_t stream) {
+  pfkv_kv_dtype dtype;
+  int scale_stride;
+  if (!split_dtype(dtype_arg, &dtype, &scale_stride))
+    return fail(PFKV_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(dtype_arg));
+  Plan pl;
+  pfkv_status st = make_plan(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype, mask,
+                             window, max_seq_len, num_splits, &pl);
+  if (st != PFKV_OK) return st;
+  if (num_seqs == 0) return PFKV_OK;
+  if (!out || !lse || !q || !k_cache || !v_cache || !block_table || !seq_lens)
+    return fail(PFKV_ERR_INVALID_ARG, "null pointer");
+  if (dtype != PFKV_KV_FP16 && (!k_scale || !v_scale)) return fail(PFKV_ERR_INVALID_ARG, "null scale pointer");
+  if (num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return fail(PFKV_ERR_INVALID_ARG, "num_blocks=%d max_blocks_per_seq=%d", num_blocks, max_blocks_per_seq);
+  const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * page_size;
+  if (rows > 0x7fffffffLL) return fail(PFKV_ERR_UNSUPPORTED, "cache pool of %lld rows exceeds 2^31", rows);
+  if (static_cast<long long>(max_blocks_per_seq) * page_size > 0x7fffffffLL)
+    return fail(PFKV_ERR_UNSUPPORTED, "max_blocks_per_seq * page_size exceeds 2^31");
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15)
+    return fail(PFKV_ERR_INVALID_ARG, "cache pools must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 7)
+    return fail(PFKV_ERR_INVALID_ARG, "q and out must be 8-byte aligned");
+  if (reinterpret_cast<uintptr_t>(lse) & 3) return fail(PFKV_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  const size_t need = workspace_for(pl, num_seqs, num_q_tokens, num_q_heads, head_dim);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need)
+      return fail(PFKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) & 15)
+      return fail(PFKV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  }
+  int dev;
+  unsigned* err;
+  cudaError_t e = current_device(&dev);
+  if (e == cudaSuccess) e = err_word(dev, &err);
+  if (e != cudaSuccess) return cuda_fail(e, "device set-up");
+
+  CUtensorMap tmk, tmv;
+  const int kv = kv_of(dtype);
+  st = tensor_map(dev, k_cache, kv, head_dim, page_size, rows, &tmk);
+  if (st != PFKV_OK) return st;
+  st = tensor_map(dev, v_cache, kv, head_dim, page_size, rows, &tmv);
+  if (st != PFKV_OK) return st;
+
+  DecodeParams p;
+  p.q = static_cast<const __half*>(q);
+  p.out = static_cast<__half*>(out);
+  p.lse = lse;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.scale_stride = scale_stride;
+  const size_t nrows = static_cast<size_t>(num_seqs) * num_q_tokens * num_q_heads;
+  p.o_part = need ? static_cast<float*>(workspace) : nullptr;
+  p.lse_part = need ? static_cast<float*>(workspace) + nrows * pl.splits * head_dim : nullptr;
+  p.err = err;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.T = num_q_tokens;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.G = num_q_heads / num_kv_heads;
+  p.page_size = page_size;
+  p.page_shift = log2i(page_size);
+  p.num_blocks = num_blocks;
+  p.max_seq_len = max_seq_len;
+  p.split_tokens = pl.split_tokens;
+  p.num_splits = pl.splits;
+  p.nrg = pl.nrg;
+  p.nts = pl.nts;
+  p.softmax_scale = softmax_scale;
+  p.causal = pl.causal;
+  p.window = pl.window;
+  p.slab_tokens = pl.slab_tokens;
+  p.num_slabs = pl.num_slabs;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  dim3 grid(pl.splits, num_kv_heads * pl.num_slabs, num_seqs);
+  if (pl.tc) {
+    e = kv == kKvE4m3 ? launch_verify_e4m3(head_dim, pl.nmax, tmk, tmv, p, grid, s, nullptr)
+                      : launch_verify_e5m2(head_dim, pl.nmax, tmk, tmv, p, grid, s, nullptr);
+  } else {
+    e = kv == kKvFp16 ? launch_decode_fp16(pl.cfg, tmk, tmv, p, grid, s)
+                      : (kv == kKvE4m3 ? launch_decode_e4m3(pl.cfg, tmk, tmv, p, grid, s)
+                                       : launch_decode_e5m2(pl.cfg, tmk, tmv, p, grid, s));
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  if (pl.splits > 1) {
+    const long long cap_ll = static_cast<long long>(max_blocks_per_seq) * page_size;
+    MergeRows mr;
+    mr.seq_lens = seq_lens;
+    mr.T = num_q_tokens;
+    mr.num_q_heads = num_q_heads;
+    mr.slab_tokens = pl.slab_tokens;
+    mr.causal = pl.causal;
+    mr.window = pl.window;
+    mr.tile = pl.tile;
+    mr.split_tokens = pl.split_tokens;
+    mr.len_cap = static_cast<int>(cap_ll < max_seq_len ? cap_ll : max_seq_len);
+    e = launch_lse_merge(p.out, lse, p.o_part, p.lse_part, static_cast<int>(nrows), pl.splits, head_dim, mr, s);
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  }
+  return PFKV_OK;
 }
 
 }  // namespace
@@ -331,7 +505,7 @@ uint32_t pfkv_capabilities(void) {
   return PFKV_CAP_KV_FP16 | PFKV_CAP_KV_FP8_E4M3 | PFKV_CAP_KV_FP8_E5M2 | PFKV_CAP_HEAD_DIM_128 |
          PFKV_CAP_HEAD_DIM_256 | PFKV_CAP_PAGE_16 | PFKV_CAP_PAGE_2048 | PFKV_CAP_PAGE_POW2_ANY |
          PFKV_CAP_Q_TOKENS_1_8 | PFKV_CAP_Q_TOKENS_1_16 | PFKV_CAP_SPLIT_KV |
-         PFKV_CAP_SCALES_PER_HEAD;
+         PFKV_CAP_SCALES_PER_HEAD | PFKV_CAP_NON_CAUSAL | PFKV_CAP_SLIDING_WINDOW | PFKV_CAP_PREFILL;
 }
 
 pfkv_status pfkv_device_errors(uint32_t* flags, int clear) {
@@ -412,132 +586,62 @@ pfkv_status pfkv_kv_cache_zero_blocks(void* k_cache, void* v_cache, const int32_
   return e == cudaSuccess ? PFKV_OK : cuda_fail(e, "zero_blocks launch");
 }
 
+
+pfkv_status pfkv_attention_plan(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                                int page_size, pfkv_kv_dtype dtype, int mask, int window, int max_seq_len,
+                                int num_splits_request, int* num_splits, int* split_tokens) {
+  return plan_impl(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype, mask, window,
+                   max_seq_len, num_splits_request, num_splits, split_tokens);
+}
+
+size_t pfkv_attention_workspace_bytes(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int page_size, pfkv_kv_dtype dtype, int mask, int window,
+                                      int max_seq_len, int num_splits_request) {
+  return workspace_impl(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype, mask, window,
+                        max_seq_len, num_splits_request);
+}
+
+pfkv_status pfkv_paged_attention(void* out, float* lse, const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                                 int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int page_size, int num_blocks, pfkv_kv_dtype dtype, const float* k_scale,
+                                 const float* v_scale, float softmax_scale, int mask, int window, int max_seq_len,
+                                 int num_splits, void* workspace, size_t workspace_bytes, pfkv_stream_t stream) {
+  return attention_impl(out, lse, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, num_seqs,
+                        num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, num_blocks, dtype, k_scale,
+                        v_scale, softmax_scale, mask, window, max_seq_len, num_splits, workspace, workspace_bytes,
+                        stream);
+}
+
 pfkv_status pfkv_decode_plan(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads, int head_dim,
-                             int page_size, pfkv_kv_dtype dtype_arg, int max_seq_len, int num_splits_request,
+                             int page_size, pfkv_kv_dtype dtype, int max_seq_len, int num_splits_request,
                              int* num_splits, int* split_tokens) {
-  pfkv_kv_dtype dtype;
-  int unused_stride;
-  if (!split_dtype(dtype_arg, &dtype, &unused_stride))
-    return fail(PFKV_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(dtype_arg));
-  Plan pl;
-  pfkv_status st = make_plan(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype,
-                             max_seq_len, num_splits_request, &pl);
+  pfkv_status st = check_decode_tokens(num_q_tokens, num_q_heads, num_kv_heads);
   if (st != PFKV_OK) return st;
-  if (num_splits) *num_splits = pl.splits;
-  if (split_tokens) *split_tokens = pl.split_tokens;
-  return PFKV_OK;
+  return plan_impl(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype, PFKV_MASK_CAUSAL,
+                   0, max_seq_len, num_splits_request, num_splits, split_tokens);
 }
 
 size_t pfkv_decode_workspace_bytes(int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads, int head_dim,
-                                   int page_size, pfkv_kv_dtype dtype_arg, int max_seq_len, int num_splits_request) {
-  pfkv_kv_dtype dtype;
-  int unused_stride;
-  if (!split_dtype(dtype_arg, &dtype, &unused_stride)) return 0;
-  Plan pl;
-  if (make_plan(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype, max_seq_len,
-                num_splits_request, &pl) != PFKV_OK)
-    return 0;
-  return workspace_for(pl, num_seqs, num_q_tokens, num_q_heads, head_dim);
+                                   int page_size, pfkv_kv_dtype dtype, int max_seq_len, int num_splits_request) {
+  if (check_decode_tokens(num_q_tokens, num_q_heads, num_kv_heads) != PFKV_OK) return 0;
+  return workspace_impl(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype,
+                        PFKV_MASK_CAUSAL, 0, max_seq_len, num_splits_request);
 }
 
 pfkv_status pfkv_paged_attention_decode(void* out, float* lse, const void* q, const void* k_cache, const void* v_cache,
                                         const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
                                         int num_seqs, int num_q_tokens, int num_q_heads, int num_kv_heads,
-                                        int head_dim, int page_size, int num_blocks, pfkv_kv_dtype dtype_arg,
+                                        int head_dim, int page_size, int num_blocks, pfkv_kv_dtype dtype,
                                         const float* k_scale, const float* v_scale, float softmax_scale,
                                         int max_seq_len, int num_splits, void* workspace, size_t workspace_bytes,
                                         pfkv_stream_t stream) {
-  pfkv_kv_dtype dtype;
-  int scale_stride;
-  if (!split_dtype(dtype_arg, &dtype, &scale_stride))
-    return fail(PFKV_ERR_INVALID_ARG, "unknown kv dtype %d", static_cast<int>(dtype_arg));
-  Plan pl;
-  pfkv_status st = make_plan(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype,
-                             max_seq_len, num_splits, &pl);
+  pfkv_status st = check_decode_tokens(num_q_tokens, num_q_heads, num_kv_heads);
   if (st != PFKV_OK) return st;
-  if (num_seqs == 0) return PFKV_OK;
-  if (!out || !lse || !q || !k_cache || !v_cache || !block_table || !seq_lens)
-    return fail(PFKV_ERR_INVALID_ARG, "null pointer");
-  if (dtype != PFKV_KV_FP16 && (!k_scale || !v_scale)) return fail(PFKV_ERR_INVALID_ARG, "null scale pointer");
-  if (num_blocks <= 0 || max_blocks_per_seq <= 0)
-    return fail(PFKV_ERR_INVALID_ARG, "num_blocks=%d max_blocks_per_seq=%d", num_blocks, max_blocks_per_seq);
-  const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * page_size;
-  if (rows > 0x7fffffffLL) return fail(PFKV_ERR_UNSUPPORTED, "cache pool of %lld rows exceeds 2^31", rows);
-  if (static_cast<long long>(max_blocks_per_seq) * page_size > 0x7fffffffLL)
-    return fail(PFKV_ERR_UNSUPPORTED, "max_blocks_per_seq * page_size exceeds 2^31");
-  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15)
-    return fail(PFKV_ERR_INVALID_ARG, "cache pools must be 16-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 7)
-    return fail(PFKV_ERR_INVALID_ARG, "q and out must be 8-byte aligned");
-  if (reinterpret_cast<uintptr_t>(lse) & 3) return fail(PFKV_ERR_INVALID_ARG, "lse must be 4-byte aligned");
-  const size_t need = workspace_for(pl, num_seqs, num_q_tokens, num_q_heads, head_dim);
-  if (need > 0) {
-    if (!workspace || workspace_bytes < need)
-      return fail(PFKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
-    if (reinterpret_cast<uintptr_t>(workspace) & 15)
-      return fail(PFKV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-  }
-  int dev;
-  unsigned* err;
-  cudaError_t e = current_device(&dev);
-  if (e == cudaSuccess) e = err_word(dev, &err);
-  if (e != cudaSuccess) return cuda_fail(e, "device set-up");
-
-  CUtensorMap tmk, tmv;
-  const int kv = kv_of(dtype);
-  st = tensor_map(dev, k_cache, kv, head_dim, page_size, rows, &tmk);
-  if (st != PFKV_OK) return st;
-  st = tensor_map(dev, v_cache, kv, head_dim, page_size, rows, &tmv);
-  if (st != PFKV_OK) return st;
-
-  DecodeParams p;
-  p.q = static_cast<const __half*>(q);
-  p.out = static_cast<__half*>(out);
-  p.lse = lse;
-  p.block_table = block_table;
-  p.seq_lens = seq_lens;
-  p.k_scale = k_scale;
-  p.v_scale = v_scale;
-  p.scale_stride = scale_stride;
-  const size_t nrows = static_cast<size_t>(num_seqs) * num_q_tokens * num_q_heads;
-  p.o_part = need ? static_cast<float*>(workspace) : nullptr;
-  p.lse_part = need ? static_cast<float*>(workspace) + nrows * pl.splits * head_dim : nullptr;
-  p.err = err;
-  p.max_blocks = max_blocks_per_seq;
-  p.num_seqs = num_seqs;
-  p.T = num_q_tokens;
-  p.num_q_heads = num_q_heads;
-  p.num_kv_heads = num_kv_heads;
-  p.G = num_q_heads / num_kv_heads;
-  p.page_size = page_size;
-  p.page_shift = log2i(page_size);
-  p.num_blocks = num_blocks;
-  p.max_seq_len = max_seq_len;
-  p.split_tokens = pl.split_tokens;
-  p.num_splits = pl.splits;
-  p.nrg = pl.nrg;
-  p.nts = pl.nts;
-  p.softmax_scale = softmax_scale;
-
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  dim3 grid(pl.splits, num_kv_heads, num_seqs);
-  if (pl.tc) {
-    e = kv == kKvE4m3 ? launch_verify_e4m3(head_dim, pl.nmax, tmk, tmv, p, grid, s, nullptr)
-                      : launch_verify_e5m2(head_dim, pl.nmax, tmk, tmv, p, grid, s, nullptr);
-  } else {
-    e = kv == kKvFp16 ? launch_decode_fp16(pl.cfg, tmk, tmv, p, grid, s)
-                      : (kv == kKvE4m3 ? launch_decode_e4m3(pl.cfg, tmk, tmv, p, grid, s)
-                                       : launch_decode_e5m2(pl.cfg, tmk, tmv, p, grid, s));
-  }
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  if (pl.splits > 1) {
-    const long long cap_ll = static_cast<long long>(max_blocks_per_seq) * page_size;
-    const int cap = static_cast<int>(cap_ll < max_seq_len ? cap_ll : max_seq_len);
-    e = launch_lse_merge(p.out, lse, p.o_part, p.lse_part, static_cast<int>(nrows), pl.splits, head_dim, seq_lens,
-                         num_q_tokens * num_q_heads, pl.split_tokens, max_seq_len, cap, s);
-    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
-  }
-  return PFKV_OK;
+  return attention_impl(out, lse, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, num_seqs,
+                        num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, num_blocks, dtype, k_scale,
+                        v_scale, softmax_scale, PFKV_MASK_CAUSAL, 0, max_seq_len, num_splits, workspace,
+                        workspace_bytes, stream);
 }
 
 pfkv_status pfkv_lse_merge(void* out, float* lse, const float* o_parts, const float* lse_parts, int rows,
@@ -552,8 +656,9 @@ pfkv_status pfkv_lse_merge(void* out, float* lse, const float* o_parts, const fl
     return fail(PFKV_ERR_INVALID_ARG, "o_parts must be 16-byte and out 8-byte aligned");
   if (static_cast<long long>(rows) * num_parts * head_dim > (1LL << 40))
     return fail(PFKV_ERR_INVALID_ARG, "too large");
+  MergeRows every_row = {};  // no sequence lengths: every row has num_parts parts
   cudaError_t e = launch_lse_merge(static_cast<__half*>(out), lse, o_parts, lse_parts, rows, num_parts, head_dim,
-                                   nullptr, 1, 1, 0, 0, reinterpret_cast<cudaStream_t>(stream));
+                                   every_row, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PFKV_OK : cuda_fail(e, "merge launch");
 }
 

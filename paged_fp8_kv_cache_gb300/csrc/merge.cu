@@ -13,6 +13,7 @@
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
+#include "mask_span.h"
 #include "pfkv_internal.h"
 
 namespace pfkv {
@@ -21,8 +22,7 @@ template <int D>
 __global__ void __launch_bounds__(256) lse_merge_kernel(__half* __restrict__ out, float* __restrict__ lse,
                                                         const float* __restrict__ o_parts,
                                                         const float* __restrict__ lse_parts, int rows, int num_parts,
-                                                        const int32_t* __restrict__ seq_lens, int rows_per_seq,
-                                                        int split_tokens, int len_cap) {
+                                                        const MergeRows mr) {
   // One CTA (8 warps) per row. Warp w takes parts w, w+8, ...; each lane owns D/32
   // consecutive output elements. A warp issues the loads (LSE and output) of up to kBatch of
   // its parts at once and keeps a running maximum with sums rescaled to it, so a row costs
@@ -36,14 +36,17 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(__half* __restrict__ out
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = blockIdx.x;
   int n = num_parts;
-  if (seq_lens != nullptr) {
+  if (mr.seq_lens != nullptr) {
     // The sequence lengths are read before this grid's dependency wait: they are an input of
     // the decode call, complete before the decode kernel ran, and this grid starts only once
     // every CTA of the decode kernel has passed its own wait (the partials are not).
-    int len = seq_lens[r / rows_per_seq];
-    len = len < 0 ? 0 : (len > len_cap ? len_cap : len);
-    n = len > 0 ? (len + split_tokens - 1) / split_tokens : 1;
-    if (n <= 1) return;  // written directly by the decode kernel (uniform across the CTA)
+    const int rows_per_seq = mr.T * mr.num_q_heads;
+    int len = mr.seq_lens[r / rows_per_seq];
+    len = len < 0 ? 0 : (len > mr.len_cap ? mr.len_cap : len);
+    const int t = (r / mr.num_q_heads) % mr.T;
+    const SlabSpan sp = slab_span(len, mr.T, t / mr.slab_tokens, mr.slab_tokens, mr.causal, mr.window, mr.tile);
+    n = span_splits(sp, mr.split_tokens);
+    if (n <= 1) return;  // written directly by the attention kernel (uniform across the CTA)
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const float* lp = lse_parts + static_cast<int64_t>(r) * num_parts;
@@ -172,9 +175,7 @@ __global__ void __launch_bounds__(256) lse_merge_generic_kernel(__half* __restri
 }
 
 cudaError_t launch_lse_merge(__half* out, float* lse, const float* o_parts, const float* lse_parts, int rows,
-                             int num_parts, int head_dim, const int32_t* seq_lens, int rows_per_seq,
-                             int split_tokens, int max_seq_len, int max_len_cap, cudaStream_t stream) {
-  (void)max_seq_len;
+                             int num_parts, int head_dim, const MergeRows& mr, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   if (head_dim != 128 && head_dim != 256) {
     const int64_t total = static_cast<int64_t>(rows) * (head_dim / 4);
@@ -193,13 +194,9 @@ cudaError_t launch_lse_merge(__half* out, float* lse, const float* o_parts, cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const int rps = rows_per_seq > 0 ? rows_per_seq : 1;
-  const int st = split_tokens > 0 ? split_tokens : 1;
   if (head_dim == 128)
-    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128>, out, lse, o_parts, lse_parts, rows, num_parts, seq_lens,
-                              rps, st, max_len_cap);
-  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<256>, out, lse, o_parts, lse_parts, rows, num_parts, seq_lens, rps,
-                            st, max_len_cap);
+    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128>, out, lse, o_parts, lse_parts, rows, num_parts, mr);
+  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<256>, out, lse, o_parts, lse_parts, rows, num_parts, mr);
 }
 
 }  // namespace pfkv

@@ -45,6 +45,11 @@ struct DecodeParams {
   int nrg;  // row groups (of 8*NT rows) per CTA
   int nts;  // consumer warps per row group (key slices)
   float softmax_scale;
+  // mask and query slabs (mask_span.h): grid.y = num_kv_heads * num_slabs
+  int causal;       // 1: query t sees no key after its own position
+  int window;       // > 0: query t sees no key W or more positions before its own (0: no window)
+  int slab_tokens;  // query tokens per CTA
+  int num_slabs;    // ceil(T / slab_tokens)
 };
 
 struct DecodeLaunch {
@@ -91,13 +96,17 @@ cudaError_t launch_verify_e4m3(int head_dim, int nmax, const CUtensorMap& tmk, c
 cudaError_t launch_verify_e5m2(int head_dim, int nmax, const CUtensorMap& tmk, const CUtensorMap& tmv,
                                const DecodeParams& p, dim3 grid, cudaStream_t stream, int* ctas_out);
 
-// merge.cu: combine per-range partials. If seq_lens is non-null, row r of
-// sequence b = r / (T * num_q_heads) has ceil(seq_len / split_tokens) parts
-// (rows with one part are skipped: the decode kernel wrote them); otherwise
-// every row has num_parts parts.
+// How many parts each row of an attention call has (rows of sequence b = r / (T * Hq), query
+// token (r / Hq) % T): the split ranges of its slab (mask_span.h); rows with one part are
+// skipped (the attention kernel wrote them).
+struct MergeRows {
+  const int32_t* seq_lens;  // null: every row has num_parts parts
+  int T, num_q_heads, slab_tokens, causal, window, tile, split_tokens, len_cap;
+};
+
+// merge.cu: combine per-range partials.
 cudaError_t launch_lse_merge(__half* out, float* lse, const float* o_parts, const float* lse_parts, int rows,
-                             int num_parts, int head_dim, const int32_t* seq_lens, int rows_per_seq,
-                             int split_tokens, int max_seq_len, int max_len_cap, cudaStream_t stream);
+                             int num_parts, int head_dim, const MergeRows& mr, cudaStream_t stream);
 
 // zero_blocks.cu
 cudaError_t launch_zero_blocks(void* k_cache, void* v_cache, const int32_t* block_ids, int n_ids, long long block_bytes,

@@ -4,7 +4,10 @@
 // "Production DFlash2 on V100" / "Flash-V100 long-context improvements":
 // exact grouped q8 verification over FP8 KV) form a real dense tile.
 //
-// One CTA = one (key range, KV head, sequence), 14 warps:
+// One CTA = one (key range, KV head, query slab, sequence), 14 warps (the slab
+// is all T tokens of a verify, or up to 64 rows of a prefill chunk; the mask --
+// causal or not, sliding window -- bounds each row's keys from both sides, and
+// a CTA's range starts at its slab's lowest visible key: mask_span.h):
 //   warp 0      producers: TMA tile copies of 128-key FP8 K (lane 0) and V
 //               (lane 1) tiles into two shared-memory rings (same tensor maps
 //               as the decode kernel);
@@ -51,6 +54,7 @@
 
 #include "device_utils.cuh"
 #include "frag_layout.h"
+#include "mask_span.h"
 #include "pfkv_internal.h"
 #include "verify_layout.h"
 
@@ -234,8 +238,9 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
   // derived from it stays a shared-memory pointer (32-bit shared loads and stores)
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int R = p.T * p.G;
+  const int split = blockIdx.x, b = blockIdx.z;
+  const int kvh = blockIdx.y % p.num_kv_heads;
+  const int slab = p.num_slabs - 1 - static_cast<int>(blockIdx.y) / p.num_kv_heads;  // longest slabs first
 
   // launched with programmatic stream serialisation: wait for the preceding grid first
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -243,14 +248,16 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
   {
     const int cap = min(p.max_seq_len, p.max_blocks * p.page_size);
     if (N < 0 || N > cap) {
-      if (threadIdx.x == 0 && split == 0 && kvh == 0) atomicOr(p.err, kDevErrSeqLen);
+      if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) atomicOr(p.err, kDevErrSeqLen);
       N = N < 0 ? 0 : cap;
     }
   }
-  const int nsplit_b = N > 0 ? (N + p.split_tokens - 1) / p.split_tokens : 1;
+  const SlabSpan sp = slab_span(N, p.T, slab, p.slab_tokens, p.causal, p.window, KT);
+  const int nsplit_b = span_splits(sp, p.split_tokens);
   if (split >= nsplit_b) return;
-  const int t0 = split * p.split_tokens;
-  const int t1 = min(N, t0 + p.split_tokens);
+  const int R = (sp.ts1 - sp.ts0) * p.G;  // query rows of this slab
+  const int t0 = sp.base + split * p.split_tokens;
+  const int t1 = sp.hi >= sp.lo ? min(sp.hi + 1, t0 + p.split_tokens) : t0;
   const int ntiles = t1 > t0 ? (t1 - t0 + KT - 1) / KT : 0;
 
   float* m_ref = reinterpret_cast<float*>(smem + S::OFF_MISC);  // [NMAX] reference max (log2 units)
@@ -320,8 +327,9 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
       float x[PER_LANE];
       float mx = 0.f;
       if (r < R) {
-        const int t = r / p.G, j = r - t * p.G;
-        const __half* src = p.q + ((static_cast<size_t>(b) * p.T + t) * p.num_q_heads + kvh * p.G + j) * D + lane * PER_LANE;
+        const int tl = r / p.G, j = r - tl * p.G;
+        const __half* src =
+            p.q + ((static_cast<size_t>(b) * p.T + sp.ts0 + tl) * p.num_q_heads + kvh * p.G + j) * D + lane * PER_LANE;
         if constexpr (PER_LANE == 8) {
           const uint4 v = *reinterpret_cast<const uint4*>(src);
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -655,7 +663,13 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
     float l_part[HN];  // this thread's (key lane's) share of its rows' sums, fp32
 #pragma unroll
     for (int r = 0; r < HN; ++r) l_part[r] = 0.f;
-    const int tlim_base = N - p.T;  // row r sees keys <= N - T + r / G
+    // Row r of the slab is query token ts0 + r / G at position pos0 + r / G; it sees key kp iff
+    // r >= rmin(kp) (causal: kp is not after it) and r < rmax(kp) (window: kp is less than W
+    // positions before it). Every row sees [lo_all, hi_all] (the slab's first token's upper and
+    // last token's lower bound).
+    const int pos0 = N - p.T + sp.ts0;
+    const int hi_all = key_hi(N, p.T, sp.ts0, p.causal);
+    const int lo_all = key_lo(N, p.T, sp.ts1 - 1, p.window);
     auto load8 = [](const float* src, float (&m)[8]) {
       const float4 a = *reinterpret_cast<const float4*>(src);
       const float4 c = *reinterpret_cast<const float4*>(src + 4);
@@ -682,10 +696,15 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
       tc_fence_after();
       const int tile_start = t0 + it * KT;
       const int kp = tile_start + key_lane;  // absolute key position
-      const bool in_range = kp < t1;
-      // row r sees this key iff r / G >= kp - (N - T), i.e. r >= G * (kp - (N - T))
-      const int rmin = p.G * (kp - tlim_base);
-      const bool all_vis = (tile_start + KT <= t1) && (tile_start + KT - 1 <= tlim_base);  // CTA-uniform
+      // The rows that see this key are rmin <= r < rmax: rows r >= G * (kp - pos0) have kp at or
+      // before their position, rows r < G * (kp + W - pos0) have it within their window (clamped
+      // to [0, 64]: a slab has at most 64 rows); none past the range end. Padding rows follow the
+      // same rule (they are never written out; a row that sees nothing gets p = 0).
+      const long long dk = static_cast<long long>(kp) - pos0;
+      const int rmin = p.causal ? static_cast<int>(max(0LL, min(64LL, p.G * dk))) : 0;
+      const int rmax = kp >= t1 ? 0 : (p.window > 0 ? static_cast<int>(max(0LL, min(64LL, p.G * (dk + p.window)))) : 64);
+      const bool all_vis =  // CTA-uniform: every row sees every key of the tile
+          (tile_start + KT <= t1) && (tile_start + KT - 1 <= hi_all) && (tile_start >= lo_all);
       // this key's logits of rows rbase .. rbase+HN-1 (sum of the three Q-term columns) less
       // the rows' references, x = s - m_use in base-2 units, -inf where masked; then the S^T
       // buffer goes back to the MMA warp. And whether any x exceeds its row's threshold.
@@ -714,7 +733,7 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int r = rbase + c + j;
-            const bool vis = in_range && (r >= R || r >= rmin);
+            const bool vis = r >= rmin && r < rmax;
             const float raw = (__uint_as_float(v0[j]) + __uint_as_float(v1[j])) + __uint_as_float(v2[j]);
             x[c + j] = vis ? fmaf(raw, sc[j], -mu[j]) : -CUDART_INF_F;
             exceed |= x[c + j] > th[j];
@@ -862,8 +881,8 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
       const float L = lsum[r] + lsum[NMAX + r] + lsum[2 * NMAX + r] + lsum[3 * NMAX + r];
       const float M = m_ref[r];
       const bool has = alive && ntiles > 0 && (M != kNoRef) && (L > 0.f);
-      const int t = r / p.G, jj = r - t * p.G;
-      const int grow = (b * p.T + t) * p.num_q_heads + kvh * p.G + jj;
+      const int tl = r / p.G, jj = r - tl * p.G;
+      const int grow = (b * p.T + sp.ts0 + tl) * p.num_q_heads + kvh * p.G + jj;
       rscale[r] = has ? vscale / L : 0.f;
       out_row[r] = grow;
       const float lse_val = has ? (M + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;

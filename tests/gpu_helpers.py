@@ -67,6 +67,23 @@ class GpuCase:
         self.last_workspace = ws
         return out, lse
 
+    def attention(self, causal=True, window=0, num_splits=0, max_seq_len=None):
+        """pfkv_paged_attention over the whole case (any number of query tokens, a mask choice)."""
+        s = self.case.spec
+        msl = int(self.case.seq_lens.max()) if max_seq_len is None else max_seq_len
+        B = self.seq_lens.shape[0]
+        T = s.num_q_tokens
+        out = torch.full(self.q.shape, float("nan"), dtype=torch.float16, device=DEV)
+        lse = torch.full(self.q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+        ws_bytes = pf.pfkv_attention_workspace_bytes(B, T, s.num_q_heads, s.num_kv_heads, s.head_dim, s.page_size,
+                                                     s.kv_dtype, msl, causal, window, num_splits)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=DEV)
+        pf.pfkv_paged_attention(out, lse, self.q, self.k_cache, self.v_cache, self.block_table, self.seq_lens, T,
+                                s.num_kv_heads, s.page_size, s.kv_dtype, self.k_scale, self.v_scale,
+                                float(self.case.softmax_scale), msl, causal, window, num_splits, ws)
+        self.last_workspace = ws
+        return out, lse
+
 
 def assert_close(out, lse, o_ref, l_ref, rows=None, out_tol=2e-3, lse_tol=1e-4):
     o = out.float().cpu().numpy().astype(np.float64)

@@ -46,7 +46,7 @@ def test_status_strings_and_capabilities(pflib):
                      (3, "PFKV_ERR_WORKSPACE"), (4, "PFKV_ERR_CUDA"), (5, "PFKV_ERR_DEVICE_CHECK")]:
         assert pf.pfkv_status_string(st) == name
     caps = pf.pfkv_capabilities()
-    for bit in (0x1, 0x2, 0x4, 0x10, 0x20, 0x100, 0x200, 0x1000, 0x2000, 0x4000):
+    for bit in (0x1, 0x2, 0x4, 0x10, 0x20, 0x100, 0x200, 0x1000, 0x2000, 0x4000, 0x10000, 0x20000, 0x40000):
         assert caps & bit
 
 
@@ -86,6 +86,42 @@ def test_split_plan_with_explicit_count(pflib, msl, req, exp):
     assert pf.pfkv_decode_plan(4, 1, 32, 8, 128, 16, "e4m3", msl, req) == exp
     S, C = exp
     assert S * C >= msl and (S - 1) * C < max(msl, 1)
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(T=8193), pf.PFKV_ERR_UNSUPPORTED),     # more query tokens than one call takes
+    (dict(Hq=65, Hkv=1), pf.PFKV_ERR_UNSUPPORTED),  # one token's heads must fit a 64-row slab
+    (dict(mask=2), pf.PFKV_ERR_INVALID_ARG),
+    (dict(window=-1), pf.PFKV_ERR_INVALID_ARG),
+])
+def test_attention_plan_rejects_bad_arguments(pflib, args, status):
+    a = dict(B=1, T=8, Hq=24, Hkv=4, D=256, P=2048, kv=2, mask=1, window=0, msl=262144, S=4)
+    a.update(args)
+    lib = pf.load()
+    ns, st = ctypes.c_int(0), ctypes.c_int(0)
+    got = lib.pfkv_attention_plan(a["B"], a["T"], a["Hq"], a["Hkv"], a["D"], a["P"], a["kv"], a["mask"], a["window"],
+                                  a["msl"], a["S"], ctypes.byref(ns), ctypes.byref(st))
+    assert got == status
+
+
+@pytest.mark.parametrize("T,causal,window,req,exp", [
+    (8, True, 0, 19, (19, 13824)),      # the q8 verify: ranges over the whole sequence
+    (8, False, 4096, 5, (5, 896)),      # a window: ranges over window + block + one tile only
+    (8, True, 4096, 2, (2, 2176)),
+    (2048, True, 0, 1, (1, 262144)),    # a prefill chunk of 2048 tokens, 10-token slabs
+    (2048, True, 0, 3, (3, 87424)),
+])
+def test_attention_plan_spans(pflib, T, causal, window, req, exp):
+    # explicit split counts need no device query (E5M2, group of 6: the tcgen05 kernel, 128-key tiles)
+    assert pf.pfkv_attention_plan(1, T, 24, 4, 256, 2048, "e5m2", 262144, causal, window, req) == exp
+
+
+def test_decode_entry_points_keep_their_token_limit(pflib):
+    with pytest.raises(pf.PfkvError) as ei:
+        pf.pfkv_decode_plan(1, 17, 8, 8, 128, 16, "e4m3", 4096, 2)
+    assert ei.value.status == pf.PFKV_ERR_UNSUPPORTED
+    assert pf.pfkv_decode_workspace_bytes(1, 17, 8, 8, 128, 16, "e4m3", 4096, 2) == 0
+    assert pf.pfkv_attention_plan(1, 17, 8, 8, 128, 16, "e4m3", 4096, True, 0, 2) == (2, 2048)
 
 
 def test_decode_validation_before_any_launch(pflib):

@@ -43,8 +43,10 @@ def run(att, case, kc, vc, **kw):
     return att(**args)
 
 
-def brute(case, kc, vc):
-    """Plain loops over (b, t, h, key, d); shares nothing with the vectorised oracle."""
+def brute(case, kc, vc, causal=True, window=0):
+    """Plain loops over (b, t, h, key, d); shares nothing with the vectorised oracle. A key j
+    is visible to query t (position p = n - T + t) when it is not after p (if causal) and not
+    W or more positions before it (with a window of W keys)."""
     s = case.spec
     T, Hq, Hkv, D, P = s.num_q_tokens, s.num_q_heads, s.num_kv_heads, s.head_dim, s.page_size
     g = Hq // Hkv
@@ -66,7 +68,8 @@ def brute(case, kc, vc):
                 ks = float(ksa[kvh % ksa.size])  # one scale per pool, or KV head kvh's
                 vs = float(vsa[kvh % vsa.size])
                 qv = [float(case.q[b * T + t, h, d]) for d in range(D)]
-                keys = list(range(0, n - T + t + 1))
+                p = n - T + t
+                keys = [j for j in range(n) if (not causal or j <= p) and (window == 0 or p - j < window)]
                 if not keys:
                     out[b * T + t, h] = 0.0
                     lse[b * T + t, h] = -math.inf
@@ -98,6 +101,18 @@ BRUTE_CASES = [
 ]
 
 
+# (case, causal, window): the draft masks (sliding window, non-causal) and a prefill-length T
+BRUTE_MASK_CASES = [
+    (dict(kv="e4m3", T=3, g=2, D=8, P=4, contexts=(19, 7)), False, 0),
+    (dict(kv="e5m2", T=8, g=2, D=4, P=4, contexts=(30, 11)), False, 5),
+    (dict(kv="fp16", T=4, g=1, D=4, P=16, contexts=(26, 4)), True, 3),
+    (dict(kv="e4m3", T=8, g=3, D=4, P=4, contexts=(17,)), True, 1),
+    (dict(kv="e5m2", T=16, g=2, D=4, P=4, contexts=(40, 18)), False, 9),
+    (dict(kv="e4m3", T=40, g=2, D=4, P=16, contexts=(61, 40)), True, 0),   # a chunk of 40 prompt tokens
+    (dict(kv="e5m2", T=40, g=1, D=4, P=4, contexts=(50,)), True, 13),
+]
+
+
 def pin_brute(att):
     for c in BRUTE_CASES:
         case = workloads.make_case(tiny_spec(**dict(c)))
@@ -106,6 +121,80 @@ def pin_brute(att):
         bo, bl = brute(case, kc, vc)
         if not (np.allclose(o, bo, rtol=0, atol=1e-12) and np.allclose(l, bl, rtol=0, atol=1e-12)):
             return False
+    for c, causal, window in BRUTE_MASK_CASES:
+        case = workloads.make_case(tiny_spec(**dict(c)))
+        kc, vc = oracle_caches(case)
+        o, l = run(att, case, kc, vc, causal=causal, window=window)
+        bo, bl = brute(case, kc, vc, causal=causal, window=window)
+        if not (np.allclose(o, bo, rtol=0, atol=1e-12) and np.allclose(l, bl, rtol=0, atol=1e-12)):
+            return False
+    return True
+
+
+# Visible key sets of a 10-key sequence with 3 query tokens (positions 7, 8, 9), written out by
+# hand for each mask: (causal, window) -> one set per query token.
+VISIBLE_SETS_N10_T3 = {
+    (True, 0): [set(range(0, 8)), set(range(0, 9)), set(range(0, 10))],
+    (True, 4): [{4, 5, 6, 7}, {5, 6, 7, 8}, {6, 7, 8, 9}],
+    (True, 1): [{7}, {8}, {9}],
+    (False, 0): [set(range(10))] * 3,
+    (False, 4): [{4, 5, 6, 7, 8, 9}, {5, 6, 7, 8, 9}, {6, 7, 8, 9}],
+    (False, 1): [{7, 8, 9}, {8, 9}, {9}],
+    (False, 12): [set(range(10))] * 3,
+}
+
+
+def pin_visible_sets(att):
+    """Zero K (equal weights) and one-hot V (key j's V is the unit vector e_j): each output row is
+    the indicator of its visible keys divided by their number, and lse = ln(number)."""
+    case = workloads.make_case(tiny_spec("fp16", T=3, g=1, Hkv=1, D=16, P=4, contexts=(10,)))
+    kc, vc = oracle_caches(case)
+    kc[:] = 0
+    vc[:] = 0
+    for j in range(10):
+        vc[case.block_table[0, j // 4], 0, j % 4, j] = 1.0
+    for (causal, window), sets in VISIBLE_SETS_N10_T3.items():
+        o, l = run(att, case, kc, vc, causal=causal, window=window)
+        for t, vis in enumerate(sets):
+            want = np.zeros(16)
+            want[sorted(vis)] = 1.0 / len(vis)
+            if not (np.allclose(o[t, 0], want, rtol=0, atol=1e-15) and math.isclose(l[t, 0], math.log(len(vis)))):
+                return False
+    return True
+
+
+def pin_mask_reductions(att):
+    """A causal window at least as long as the sequence is no window; non-causal rows all see the
+    whole sequence, i.e. each is a one-token decode at the last position; a causal windowed row
+    is that query's one-token decode restricted to its last W keys."""
+    case = workloads.make_case(tiny_spec("e5m2", T=4, g=2, P=4, contexts=(23, 9)))
+    kc, vc = oracle_caches(case)
+    o, l = run(att, case, kc, vc)
+    ow, lw = run(att, case, kc, vc, window=23)
+    if not (np.array_equal(o, ow) and np.array_equal(l, lw)):
+        return False
+    onc, lnc = run(att, case, kc, vc, causal=False)
+    T = 4
+    for t in range(T):
+        q1 = case.q.reshape(case.B, T, *case.q.shape[1:])[:, t]
+        o1, l1 = run(att, case, kc, vc, q=q1, num_q_tokens=1)
+        if not (np.allclose(o1, onc.reshape(case.B, T, *o.shape[1:])[:, t], rtol=0, atol=1e-14)
+                and np.allclose(l1, lnc.reshape(case.B, T, -1)[:, t], rtol=0, atol=1e-14)):
+            return False
+    W = 3
+    ocw, lcw = run(att, case, kc, vc, window=W)
+    for b in range(case.B):
+        n = int(case.seq_lens[b])
+        for t in range(T):
+            p = n - T + t
+            if p < 0:
+                continue
+            q1 = case.q[b * T + t:b * T + t + 1]
+            o1, l1 = run(att, case, kc, vc, q=q1, num_q_tokens=1, seq_lens=np.array([p + 1], np.int32),
+                         block_table=case.block_table[b:b + 1], token_range=(p - W + 1, p + 1))
+            if not (np.allclose(o1[0], ocw[b * T + t], rtol=0, atol=1e-14)
+                    and np.allclose(l1[0], lcw[b * T + t], rtol=0, atol=1e-14)):
+                return False
     return True
 
 
@@ -214,8 +303,25 @@ def pin_split_merge(att):
     return True
 
 
+def pin_long_chunk_rows_are_shorter_decodes(att):
+    """A prefill chunk of 200 query tokens: causal row t is the one-token decode of the sequence
+    cut after position n - T + t (sampled rows)."""
+    T = 200
+    case = workloads.make_case(tiny_spec("e4m3", T=T, g=2, D=8, P=16, contexts=(260,)))
+    kc, vc = oracle_caches(case)
+    pick = [0, 1, 57, 123, 198, 199]
+    o, l = run(att, case, kc, vc, tokens=pick)
+    for t in pick:
+        q1 = case.q[t:t + 1]
+        o1, l1 = run(att, case, kc, vc, q=q1, num_q_tokens=1, seq_lens=case.seq_lens - (T - 1 - t))
+        if not (np.allclose(o1[0], o[t], rtol=0, atol=1e-14) and np.allclose(l1[0], l[t], rtol=0, atol=1e-14)):
+            return False
+    return bool(np.isnan(o[2]).all())  # rows not asked for stay NaN
+
+
 PINS = [pin_brute, pin_page_permutation, pin_constant_v, pin_zero_k, pin_single_key,
-        pin_causal_rows_are_shorter_decodes, pin_gqa_head_alone, pin_split_merge]
+        pin_causal_rows_are_shorter_decodes, pin_gqa_head_alone, pin_split_merge, pin_visible_sets,
+        pin_mask_reductions, pin_long_chunk_rows_are_shorter_decodes]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -249,8 +355,15 @@ MUTANTS = {
     "drop v_scale": ("[lo - base:hi - base] * vs", "[lo - base:hi - base]"),
     "drop softmax scale": ("s = sm * (qrows @ K.T)", "s = (qrows @ K.T)"),
     "causal off by one": ("j[None, :] <= last[:, None]", "j[None, :] < last[:, None]"),
-    "reversed draft order": ("last = np.array([n - T + t", "last = np.array([n - 1 - t"),
-    "rows head-major vs limits token-major": ("for t in range(T) for _ in heads", "for _ in heads for t in range(T)"),
+    "reversed draft order": ("pos = np.array([n - T + t", "pos = np.array([n - 1 - t"),
+    "rows head-major vs limits token-major": ("for t in toks for _ in heads", "for _ in heads for t in toks"),
+    "window off by one": ("np.maximum(0, pos - window + 1)", "np.maximum(0, pos - window)"),
+    "window ignored": ("first = np.maximum(0, pos - window + 1) if window > 0",
+                       "first = np.zeros(nt * g, dtype=np.int64) if window > 0"),
+    "window anchored at the block end": ("np.maximum(0, pos - window + 1)", "np.maximum(0, n - window + 0 * pos)"),
+    "non-causal mask still causal": ("last = pos if causal else np.full(nt * g, n - 1)", "last = pos"),
+    "non-causal bound one short": ("np.full(nt * g, n - 1)", "np.full(nt * g, n - 2)"),
+    "token subset takes the first rows": ("[toks]  # [nt, g, D]", "[:len(toks)]  # [nt, g, D]"),
     "interleaved GQA map": ("heads = list(range(kvh * g, (kvh + 1) * g))", "heads = list(range(kvh, Hq, num_kv_heads))"),
     "pages taken in sorted order": ("pages = np.asarray(block_table[b, first_page:last_page + 1], dtype=np.int64)",
                                     "pages = np.sort(np.asarray(block_table[b, first_page:last_page + 1], dtype=np.int64))"),
