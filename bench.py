@@ -83,17 +83,43 @@ class L2Flush:
         self.torch.sum(self.r, dim=0, out=self.sink)
 
 
+def visible_span(spec, n: int):
+    """Keys [lo, hi] some query row of a sequence of n keys sees under the workload's mask (its
+    query tokens sit at positions n - T .. n - 1; a window of W keys ends each row's view W
+    positions back from it)."""
+    T = spec.num_q_tokens
+    lo = max(0, n - T - spec.window + 1) if spec.window > 0 else 0
+    return lo, n - 1
+
+
+def useful_flops(case) -> int:
+    """QK^T and PV multiply-adds of every query row over its visible keys: 4 * D per (row, key)."""
+    s = case.spec
+    T, W = s.num_q_tokens, s.window
+    total = 0
+    for n in case.seq_lens.astype(np.int64):
+        p = n - T + np.arange(T)
+        hi = np.minimum(p, n - 1) if s.causal else np.full(T, n - 1)
+        lo = np.maximum(0, p - W + 1) if W > 0 else np.zeros(T, np.int64)
+        total += int(np.maximum(0, hi - lo + 1).sum())
+    return 4 * s.head_dim * s.num_q_heads * total
+
+
 def algorithmic_bytes(case, with_append: bool) -> int:
     s = case.spec
     elt = 2 if s.kv_dtype == "fp16" else 1
-    sl = case.seq_lens.astype(np.int64)
-    kv = int(sl.sum()) * s.num_kv_heads * s.head_dim * elt * 2
+    keys = pages = 0
+    for n in case.seq_lens.astype(np.int64):
+        lo, hi = visible_span(s, int(n))
+        if hi >= lo:
+            keys += hi - lo + 1
+            pages += hi // s.page_size - lo // s.page_size + 1
+    kv = keys * s.num_kv_heads * s.head_dim * elt * 2
     rows = case.B * s.num_q_tokens * s.num_q_heads
     q_out = rows * s.head_dim * 2 * 2
     lse = rows * 4
-    pages = int((-(-sl // s.page_size)).sum()) * 4
     meta = case.B * 4
-    total = kv + q_out + lse + pages + meta
+    total = kv + q_out + lse + pages * 4 + meta
     if with_append and case.slot_new.size:
         n = case.slot_new.size
         total += n * s.num_kv_heads * s.head_dim * (2 * 2 + elt * 2) + n * 8
@@ -102,9 +128,11 @@ def algorithmic_bytes(case, with_append: bool) -> int:
 
 def kernel_of(spec) -> str:
     """The kernel a workload's decode call runs: the tcgen05 grouped verifier for FP8 caches with
-    more than 16 query rows per KV head, the mma.sync decode kernel otherwise."""
-    rows = spec.num_q_tokens * (spec.num_q_heads // spec.num_kv_heads)
-    return "verify_kernel" if spec.kv_dtype != "fp16" and rows > 16 else "decode_kernel"
+    more than 16 query rows per CTA (a slab holds up to 64 rows), the mma.sync decode kernel
+    otherwise."""
+    g = spec.num_q_heads // spec.num_kv_heads
+    tokens = spec.num_q_tokens if spec.num_q_tokens * g <= 64 else 64 // g
+    return "verify_kernel" if spec.kv_dtype != "fp16" and tokens * g > 16 else "decode_kernel"
 
 
 def kernel_source_hash(kernel: str = "decode_kernel") -> str:
@@ -122,6 +150,20 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def measured_tensor_peak():
+    """Dense bf16 tensor-core TFLOP/s (burst) measured on this machine, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured"
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def profiled_traffic(workload_id: int, kernel: str):
@@ -267,11 +309,11 @@ class DeviceWorkload:
         self.h_out = torch.empty(total, dtype=torch.uint8).pin_memory()
         self.out = self.d_out[o_out:o_out + rows * s.head_dim * 2].view(torch.float16).view(B * T, Hq, s.head_dim)
         self.lse = self.d_out[o_lse:o_lse + rows * 4].view(torch.float32).view(B * T, Hq)
-        ws = pf.pfkv_decode_workspace_bytes(B, T, Hq, s.num_kv_heads, s.head_dim, s.page_size, s.kv_dtype,
-                                            self.max_seq_len, 0)
+        ws = pf.pfkv_attention_workspace_bytes(B, T, Hq, s.num_kv_heads, s.head_dim, s.page_size, s.kv_dtype,
+                                               self.max_seq_len, s.causal, s.window, 0)
         self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
-        self.splits, self.split_tokens = pf.pfkv_decode_plan(B, T, Hq, s.num_kv_heads, s.head_dim, s.page_size,
-                                                             s.kv_dtype, self.max_seq_len, 0)
+        self.splits, self.split_tokens = pf.pfkv_attention_plan(B, T, Hq, s.num_kv_heads, s.head_dim, s.page_size,
+                                                                s.kv_dtype, self.max_seq_len, s.causal, s.window, 0)
         self.has_append = case.slot_new.size > 0
         merge = self.splits > 1 and ws > 0
         self.launches_per_step = (1 if self.has_append else 0) + 1 + (1 if merge else 0)
@@ -284,10 +326,10 @@ class DeviceWorkload:
 
     def decode_step(self):
         s = self.case.spec
-        self.pf.pfkv_paged_attention_decode(self.out, self.lse, self.d["q"], self.k_cache, self.v_cache,
-                                            self.d["bt"], self.d["sl"], s.num_q_tokens, s.num_kv_heads, s.page_size,
-                                            s.kv_dtype, self.k_scale, self.v_scale,
-                                            float(self.case.softmax_scale), self.max_seq_len, 0, self.ws)
+        self.pf.pfkv_paged_attention(self.out, self.lse, self.d["q"], self.k_cache, self.v_cache, self.d["bt"],
+                                     self.d["sl"], s.num_q_tokens, s.num_kv_heads, s.page_size, s.kv_dtype,
+                                     self.k_scale, self.v_scale, float(self.case.softmax_scale), self.max_seq_len,
+                                     s.causal, s.window, 0, self.ws)
 
     def h2d(self):
         self.d_in.copy_(self.h_in, non_blocking=True)
@@ -336,10 +378,26 @@ def dtype_label(spec) -> str:
     return f"f16 mma / f32 accumulate over {kv} KV"
 
 
+def is_prefill(spec) -> bool:
+    return spec.num_q_tokens > 16
+
+
 def roofline_obj(case, wid, dec_ms, peak, peak_kind):
-    """The decode call (decode/verify kernel + merge) against the HBM copy peak."""
+    """The decode call (decode/verify kernel + merge) against the HBM copy peak; a prefill chunk
+    (dense: thousands of query rows per key) against the measured bf16 tensor peak."""
     kernel = kernel_of(case.spec)
     dec_avg = sum(dec_ms) / len(dec_ms)
+    if is_prefill(case.spec):
+        tpeak, tkind = measured_tensor_peak()
+        fl = useful_flops(case)
+        ach = fl / (dec_avg * 1e-3) / 1e12
+        return {"bound": "tensor", "kernel": f"{kernel} + lse_merge_kernel (one attention call)",
+                "achieved": round(ach, 2), "peak": tpeak, "unit": "TFLOP/s", "frac": round(ach / tpeak, 4),
+                "peak_source": f"{tkind} (MEASURED_PEAKS.json bf16_tflops, burst): the PV product runs on f16; "
+                               "QK^T runs on FP8 with Q as three E4M3 terms (1.5x the bf16-equivalent MMA work)",
+                "traffic": profiled_traffic(wid, kernel), "useful_flops_per_launch": fl,
+                "avg_launch_ms": round(dec_avg, 5),
+                "median_launch_frac": round(fl / (statistics.median(dec_ms) * 1e-3) / 1e12 / tpeak, 4)}
     dec_bytes = algorithmic_bytes(case, with_append=False)
     achieved = dec_bytes / (dec_avg * 1e-3) / 1e9
     return {"bound": "hbm", "kernel": f"{kernel} + lse_merge_kernel (one decode call)",
@@ -480,6 +538,11 @@ def per_config(torch, pf, flush, skip, peak, peak_kind, args, configs, k):
             "gpu_launches": r["launches"] * k,
             "cpu_baseline": cpu,
         }
+        if is_prefill(spec):
+            fl = useful_flops(case)
+            res[str(cid)]["tflops"] = {"value": round(fl * k / (r["total_ms"] * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                                       "useful_flops_per_step": fl,
+                                       "note": "useful causal QK^T + PV flops of the step (append included in the time)"}
         del case
     return res
 
@@ -540,16 +603,19 @@ def zero_blocks_measure(torch, pf, flush, peak, args):
 # worker builds the whole (up to 1 GB) workload.
 
 PIECE_KEYS = 8192
+PIECE_TOKENS = 16  # query tokens of a prefill chunk a piece evaluates
 _OW = None
 
 
 def _piece_arrays(case, b, kvh):
-    """fp16 K/V rows of one unit's last PIECE_KEYS keys (page-aligned start), its Q rows, scales."""
+    """One unit's piece: fp16 K/V rows of its last <= PIECE_KEYS visible keys (page-aligned start),
+    its Q rows, scales and mask; for a prefill chunk a spread of PIECE_TOKENS of its query tokens."""
     s = case.spec
     P, T, D = s.page_size, s.num_q_tokens, s.head_dim
     g = s.num_q_heads // s.num_kv_heads
     n = int(case.seq_lens[b])
-    lo = max(0, n - PIECE_KEYS) // P * P
+    lo_vis, _ = visible_span(s, n)
+    lo = max(0, n - PIECE_KEYS, lo_vis) // P * P
     pos = np.arange(lo, n)
     cached = int(case.cached[b])
     start = int(np.concatenate([[0], np.cumsum(case.cached.astype(np.int64))])[b])
@@ -564,9 +630,16 @@ def _piece_arrays(case, b, kvh):
         v16[~fill] = case.v_new[idx, kvh]
     ks = np.asarray(case.k_scale, np.float32).reshape(-1)
     vs = np.asarray(case.v_scale, np.float32).reshape(-1)
+    tokens = np.unique(np.linspace(0, T - 1, PIECE_TOKENS).astype(np.int64)) if is_prefill(s) else np.arange(T)
+    # useful flops of the piece: 4 * D per (row, visible key in [lo, n))
+    p_t = n - T + tokens
+    hi_t = np.minimum(p_t, n - 1) if s.causal else np.full(tokens.size, n - 1)
+    lo_t = np.maximum(lo, np.maximum(0, p_t - s.window + 1) if s.window > 0 else 0)
+    flops = 4 * D * g * int(np.maximum(0, hi_t - lo_t + 1).sum())
     return {"q": case.q[b * T:(b + 1) * T, kvh * g:(kvh + 1) * g, :], "k16": k16, "v16": v16,
             "ks": ks[kvh % ks.size], "vs": vs[kvh % vs.size], "sm": np.float32(case.softmax_scale),
-            "lo": lo, "n": n, "T": T, "P": P, "kv": np.array(s.kv_dtype)}
+            "lo": lo, "n": n, "T": T, "P": P, "kv": np.array(s.kv_dtype), "causal": s.causal, "window": s.window,
+            "tokens": tokens, "all_tokens": not is_prefill(s), "keys": n - max(lo, lo_vis), "flops": flops}
 
 
 def _oracle_init(tmpdir, npieces, counter, ready):
@@ -591,7 +664,10 @@ def _oracle_init(tmpdir, npieces, counter, ready):
     bt = np.full((1, (n - 1) // P + 1 if n > 0 else 1), -1, np.int32)
     bt[0, lo // P:lo // P + npages] = np.arange(npages, dtype=np.int32)
     _OW = {"q": d["q"], "kc": kc, "vc": vc, "bt": bt, "sl": np.array([n], np.int32), "T": int(d["T"]), "P": P,
-           "kv": kv, "ks": float(d["ks"]), "vs": float(d["vs"]), "sm": float(d["sm"]), "lo": lo, "n": n}
+           "kv": kv, "ks": float(d["ks"]), "vs": float(d["vs"]), "sm": float(d["sm"]), "lo": lo, "n": n,
+           "causal": bool(d["causal"]), "window": int(d["window"]),
+           "tokens": None if bool(d["all_tokens"]) else [int(t) for t in d["tokens"]],
+           "keys": int(d["keys"]), "flops": int(d["flops"])}
     with ready.get_lock():
         ready.value += 1
 
@@ -600,8 +676,9 @@ def _oracle_task(_):
     from oracle import attention as oatt
     w = _OW
     oatt.paged_attention(w["q"], w["kc"], w["vc"], w["bt"], w["sl"], w["T"], 1, w["P"], w["kv"], w["ks"], w["vs"],
-                         w["sm"], units=[(0, 0)], token_range=(w["lo"], w["n"]))
-    return w["n"] - w["lo"]
+                         w["sm"], units=[(0, 0)], token_range=(w["lo"], w["n"]), causal=w["causal"],
+                         window=w["window"], tokens=w["tokens"])
+    return w["keys"], w["flops"]
 
 
 class OracleSampler:
@@ -622,7 +699,7 @@ class OracleSampler:
         self.piece_keys = []
         for i, (b, h) in enumerate(pick):
             arr = _piece_arrays(case, b, h)
-            self.piece_keys.append(int(arr["n"] - arr["lo"]))
+            self.piece_keys.append(int(arr["keys"]))
             np.savez(os.path.join(self.tmpdir, f"piece{i}.npz"), **arr)
         self.npieces = len(pick)
         ctx = mp.get_context("spawn")
@@ -638,25 +715,32 @@ class OracleSampler:
         elt = 2 if s.kv_dtype == "fp16" else 1
         self.key_bytes = s.head_dim * elt * 2  # K + V bytes of one key of one unit
         step_bytes = algorithmic_bytes(case, case.slot_new.size > 0)
-        self.overhead = step_bytes / max(1, case.kv_bytes())  # algorithmic bytes per KV byte of a step
+        kv_visible = algorithmic_bytes(case, False) - case.B * s.num_q_tokens * s.num_q_heads * (s.head_dim * 4 + 4)
+        self.overhead = step_bytes / max(1, kv_visible)  # algorithmic bytes per visible KV byte of a step
 
     def run(self, budget_s):
-        """Evaluate pieces for about budget_s; effective GB/s of the oracle."""
-        keys, t_total, evals = 0, 0.0, 0
+        """Evaluate pieces for about budget_s; effective GB/s (and TFLOP/s) of the oracle."""
+        keys, flops, t_total, evals = 0, 0, 0.0, 0
         while t_total < budget_s:
             t0 = time.perf_counter()
-            keys += sum(self.pool.map(_oracle_task, range(self.cores), chunksize=1))
+            res = self.pool.map(_oracle_task, range(self.cores), chunksize=1)
             t_total += time.perf_counter() - t0
+            keys += sum(r[0] for r in res)
+            flops += sum(r[1] for r in res)
             evals += self.cores
         nbytes = keys * self.key_bytes * self.overhead
         s = self.case.spec
-        return {"value": round(nbytes / t_total / 1e9, 4), "unit": "GB/s", "cores": self.cores, "kind": "oracle",
-                "sample": f"{evals} evaluations of {self.npieces} pieces of '{s.name}': one (sequence, KV head) "
-                          f"unit each, restricted to its last <= {PIECE_KEYS} keys ({min(self.piece_keys)}-"
-                          f"{max(self.piece_keys)} keys), on {self.cores} single-threaded processes, "
-                          f"{t_total:.2f} s wall; bytes scaled by the step's algorithmic/KV byte ratio "
-                          f"({self.overhead:.4f})",
-                "seconds": round(t_total, 3)}
+        rows = f"{PIECE_TOKENS} of its {s.num_q_tokens} query tokens, " if is_prefill(s) else ""
+        out = {"value": round(nbytes / t_total / 1e9, 4), "unit": "GB/s", "cores": self.cores, "kind": "oracle",
+               "sample": f"{evals} evaluations of {self.npieces} pieces of '{s.name}': one (sequence, KV head) "
+                         f"unit each, {rows}restricted to its last <= {PIECE_KEYS} visible keys "
+                         f"({min(self.piece_keys)}-{max(self.piece_keys)} keys), on {self.cores} single-threaded "
+                         f"processes, {t_total:.2f} s wall; bytes scaled by the step's algorithmic/KV byte ratio "
+                         f"({self.overhead:.4f})",
+               "seconds": round(t_total, 3)}
+        if is_prefill(s):
+            out["tflops"] = round(flops / t_total / 1e12, 6)
+        return out
 
     def close(self):
         self.pool.close()

@@ -141,31 +141,31 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
       const int P = p.page_size;
       const int* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks;
       const int page_last = (t1 - 1) >> p.page_shift;
-      // the lanes hold the ids of pages chunk_base .. chunk_base + 31 (prefetched above)
-      int chunk_base = pfirst0;
-      int my_id = 0;
-      {
-        const int mine = chunk_base + lane;
-        if (mine <= page_last) {
-          my_id = pguess == pfirst0 ? pre_id : bt[mine];
-          if (static_cast<unsigned>(my_id) >= static_cast<unsigned>(p.num_blocks)) {
-            atomicOr(p.err, kDevErrBlockId);
-            my_id = 0;
-          }
+      // The lanes hold the ids of pages chunk_base .. chunk_base + 31 (the first chunk was
+      // fetched above when it did not depend on the length), and the raw ids of the next 32
+      // pages, loaded one chunk ahead: moving to the next chunk never waits on the table (with
+      // 16-token pages a chunk lasts 8 tiles). An id outside the pool is flagged when its chunk
+      // becomes current and block 0 is read instead.
+      auto load_raw = [&](int first) -> int {
+        const int mine = first + lane;
+        return mine <= page_last ? bt[mine] : 0;
+      };
+      auto checked = [&](int raw, int first) -> int {
+        if (first + lane > page_last) return 0;
+        if (static_cast<unsigned>(raw) >= static_cast<unsigned>(p.num_blocks)) {
+          atomicOr(p.err, kDevErrBlockId);
+          return 0;
         }
-      }
+        return raw;
+      };
+      int chunk_base = pfirst0;
+      int my_id = checked(pguess == pfirst0 ? pre_id : load_raw(pfirst0), pfirst0);
+      int next_raw = load_raw(pfirst0 + 32);
       auto page_id = [&](int pidx) -> int {
         if (pidx < chunk_base || pidx >= chunk_base + 32) {
+          my_id = pidx == chunk_base + 32 ? checked(next_raw, pidx) : checked(load_raw(pidx), pidx);
           chunk_base = pidx;
-          const int mine = chunk_base + lane;
-          my_id = 0;
-          if (mine <= page_last) {
-            my_id = bt[mine];
-            if (static_cast<unsigned>(my_id) >= static_cast<unsigned>(p.num_blocks)) {
-              atomicOr(p.err, kDevErrBlockId);
-              my_id = 0;
-            }
-          }
+          next_raw = load_raw(chunk_base + 32);
         }
         return __shfl_sync(0xffffffffu, my_id, pidx - chunk_base);
       };

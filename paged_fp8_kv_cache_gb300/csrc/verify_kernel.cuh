@@ -88,6 +88,12 @@ struct VerifyShape {
   static constexpr int AV_COLS = MT * KT / 2;            // one V^T operand (fp16 pairs)
   static constexpr int NAV = COL_AV + 2 * AV_COLS <= TMEM_COLS ? 2 : 1;
   static_assert(COL_AV + NAV * AV_COLS <= TMEM_COLS, "TMEM budget");
+  // The V^T operands are written and consumed in 64-key halves: NHB half-buffers of HALF_COLS
+  // columns (M-tile mt of a half at column mt * KT / 4), so that even with room for a single
+  // 128-key operand (64 rows at D = 256) the converter writes one half while the O^T MMAs read
+  // the other.
+  static constexpr int HALF_COLS = MT * KT / 4;
+  static constexpr int NHB = 2 * NAV;
   static_assert(NQ <= 256, "MMA N");
   static_assert(HN % 8 == 0, "softmax rows come in TMEM loads of 8 columns");
   // misc: m_ref, alpha, sc2r, rscale, wred[4], lsum[4], m_use, thr, dx (NMAX floats each),
@@ -99,6 +105,7 @@ struct VerifyShape {
   static constexpr int NK = FIT / 2 > 4 ? 4 : FIT / 2;
   static constexpr int NV = FIT - NK > 4 ? 4 : FIT - NK;
   static_assert(NK >= 2 && NV >= 2, "shared memory budget");
+  static_assert(2 * NK + 2 * NV + 16 <= 32, "mbarrier slots");
   // shared memory map (offsets from the 1 KB-aligned base)
   static constexpr int OFF_KRING = 0;
   static constexpr int OFF_VRING = OFF_KRING + NK * KV_TILE;
@@ -279,9 +286,9 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
   uint64_t* kempty = kfull + NK;       // [NK] MMA commit: S^T MMAs done reading the K tile
   uint64_t* vfull = kempty + NK;       // [NV] producer -> V converter
   uint64_t* vempty = vfull + NV;       // [NV] V converter -> producer
-  uint64_t* av_full = vempty + NV;     // [NAV] V converter -> MMA (V^T operand written)
-  uint64_t* av_free = av_full + 2;     // [NAV] MMA commit: O^T MMAs done with a V^T operand
-  uint64_t* s_full = av_free + 2;      // MMA commit: S^T ready
+  uint64_t* av_full = vempty + NV;     // [NHB] V converter -> MMA (V^T half written)
+  uint64_t* av_free = av_full + 4;     // [NHB] MMA commit: O^T MMAs done with a V^T half
+  uint64_t* s_full = av_free + 4;      // MMA commit: S^T ready
   uint64_t* s_free = s_full + 1;       // softmax -> MMA: S^T read into registers
   uint64_t* pt_full = s_free + 1;      // [2] softmax -> MMA: P^T written
   uint64_t* pt_free = pt_full + 2;     // [2] MMA commit: O^T MMAs of the tile done (P^T buffer free)
@@ -300,9 +307,11 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
       mbar_init(&vfull[s], 1);
       mbar_init(&vempty[s], 4);  // one arrival per V-converter warp
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&av_full[i], 4);
+    for (int i = 0; i < S::NHB; ++i) {
+      mbar_init(&av_full[i], 4);  // one arrival per V-converter warp
       mbar_init(&av_free[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&pt_full[i], kSoftmaxWarps);
       mbar_init(&pt_free[i], 1);
     }
@@ -487,7 +496,7 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && ntiles > 0) {
-      constexpr int NAV = S::NAV;
+      constexpr int NHB = S::NHB;
       const uint32_t idesc_qk = umma_idesc_f8(S::NQ, KV == kKvE4m3 ? 0u : 1u);
       const uint32_t idesc_pv = umma_idesc_f16(NMAX);
       // descriptors of the operands' first k-slices; a k-step adds its byte offset / 16 to the
@@ -530,7 +539,10 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
         }
       }
       for (int on = 0; on < ntiles && ok; ++on) {
-        ok = mbar_wait(&av_full[on % NAV], (on / NAV) & 1) && mbar_wait(&pt_full[on & 1], (on >> 1) & 1);
+        // conversion units 2*on (keys 0-63) and 2*on + 1 (keys 64-127) of tile on; each parity
+        // wait on a half-buffer is sound for the same reason as above (units u - NHB, u, u + NHB
+        // of a half-buffer are waited for in order)
+        ok = mbar_wait(&av_full[(2 * on) % NHB], ((2 * on) / NHB) & 1) && mbar_wait(&pt_full[on & 1], (on >> 1) & 1);
         if (!ok) break;
         const int sn = on + 2;
         if (sn < ntiles) {
@@ -541,17 +553,28 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
         }
         tc_fence_after();
         const uint64_t pt = pt_desc + static_cast<uint64_t>(((on & 1) * S::PT_BYTES) >> 4);
-        const uint32_t av = tbase + S::COL_AV + (on % NAV) * S::AV_COLS;
 #pragma unroll
-        for (int ks = 0; ks < KT / 16; ++ks) {
-          const uint32_t poff = ((ks >> 2) * NMAX * 128 + (ks & 3) * 32) >> 4;
+        for (int h = 0; h < 2; ++h) {
+          const int u = 2 * on + h;
+          if (h == 1) {
+            ok = mbar_wait(&av_full[u % NHB], (u / NHB) & 1);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          const uint32_t av = tbase + S::COL_AV + (u % NHB) * S::HALF_COLS;
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
-            umma_ts(tbase + S::COL_O + mt * NMAX, av + mt * (KT / 2) + 8 * ks, pt + poff, idesc_pv,
-                    (on > 0 || ks > 0) ? 1u : 0u);
+          for (int kh = 0; kh < KT / 32; ++kh) {
+            const int ks = 4 * h + kh;  // 16-key step of the tile
+            const uint32_t poff = ((ks >> 2) * NMAX * 128 + (ks & 3) * 32) >> 4;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+              umma_ts(tbase + S::COL_O + mt * NMAX, av + mt * (KT / 4) + 8 * kh, pt + poff, idesc_pv,
+                      (on > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(&av_free[u % NHB]);
         }
+        if (!ok) break;
         umma_commit(&pt_free[on & 1]);
-        umma_commit(&av_free[on % NAV]);
       }
       if (!ok) atomicOr(p.err, kDevErrTimeout);
     }
@@ -569,25 +592,21 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
     int voff[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) voff[j] = vbx * S::SUB + swz_offset(j, vbyte >> 4) + (vbyte & 15);
-    for (int it = 0; it < ntiles; ++it) {
+    for (int it = 0; it < ntiles && alive; ++it) {
       const int s = it % NV;
-      // V^T buffer it % NAV is free once the O^T MMAs of tile it-NAV are done (sound: this thread
-      // saw that barrier's previous phase, of tile it-2*NAV, before converting tile it-NAV)
-      if (!mbar_wait(&vfull[s], (it / NV) & 1) ||
-          (it >= S::NAV && !mbar_wait(&av_free[it % S::NAV], ((it / S::NAV) - 1) & 1))) {
+      if (!mbar_wait(&vfull[s], (it / NV) & 1)) {
         alive = false;
         break;
       }
-      tc_fence_after();
       const unsigned char* Vs = smem + S::OFF_VRING + s * S::KV_TILE;
-      const uint32_t av = tq + S::COL_AV + (it % S::NAV) * S::AV_COLS;
       const int valid = min(KT, t1 - (t0 + it * KT));
+      uint32_t av = 0;
       // a full tile and the range's last, partial one take separate copies of the loop, so that
-      // the full tiles carry no per-key range checks
-      auto convert_tile = [&](auto tail_tag) {
+      // the full tiles carry no per-key range checks; keys k_lo .. k_lo + 63 go to one half-buffer
+      auto convert_half = [&](auto tail_tag, int k_lo) {
         constexpr bool kTail = decltype(tail_tag)::value;
 #pragma unroll 1
-        for (int k0 = 0; k0 < KT; k0 += 32) {
+        for (int k0 = k_lo; k0 < k_lo + KT / 2; k0 += 32) {
           const unsigned char* vrow = Vs + k0 * kBoxBytes;  // rows k0.. of the tile (k0 % 8 == 0)
           uint32_t v0[16], v1[16];
 #pragma unroll
@@ -617,22 +636,32 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
               v1[kk >> 1] = fp8x2_to_f16x2<KV>(X >> 16);
             }
           }
-          tmem_st16(av + (k0 >> 1), v0);
-          if constexpr (MT == 2) tmem_st16(av + KT / 2 + (k0 >> 1), v1);
+          tmem_st16(av + ((k0 - k_lo) >> 1), v0);
+          if constexpr (MT == 2) tmem_st16(av + KT / 4 + ((k0 - k_lo) >> 1), v1);
         }
       };
-      if (valid < KT) {
-        convert_tile(BoolTag<true>{});
-      } else {
-        convert_tile(BoolTag<false>{});
+      for (int h = 0; h < 2; ++h) {
+        const int u = 2 * it + h;  // conversion unit: half h of tile it
+        // half-buffer u % NHB is free once the O^T MMAs of unit u - NHB are done (sound: this
+        // thread saw that barrier's previous phase, of unit u - 2*NHB, before converting u - NHB)
+        if (u >= S::NHB && !mbar_wait(&av_free[u % S::NHB], ((u / S::NHB) - 1) & 1)) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        av = tq + S::COL_AV + (u % S::NHB) * S::HALF_COLS;
+        if (valid < KT) {
+          convert_half(BoolTag<true>{}, h * (KT / 2));
+        } else {
+          convert_half(BoolTag<false>{}, h * (KT / 2));
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&av_full[u % S::NHB]);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&av_full[it % S::NAV]);
-        mbar_arrive(&vempty[s]);
-      }
+      if (!alive) break;
+      if (lane == 0) mbar_arrive(&vempty[s]);
     }
     if (!alive && lane == 0) atomicOr(p.err, kDevErrTimeout);
   } else {

@@ -62,6 +62,8 @@ class CaseSpec:
     seed: int = 0
     scale_per_head: bool = False
     head_gain: tuple = ()
+    causal: bool = True  # the attention mask of the step's call (an input of the call, like T)
+    window: int = 0      # sliding window of keys (0 = none)
 
 
 # The five workloads of the benchmark (seed = 1000 + workload id).
@@ -100,6 +102,26 @@ EXTENSIONS = {
                 head_dim=256, page_size=2048, kv_dtype="e4m3", v_dist="uniform",
                 k_outlier_frac=0.01, seed=1007, scale_per_head=True, head_gain=(0.25, 1.0, 4.0, 0.5)),
 }
+
+# The draft's non-causal sliding-window attention: a block of 8 query tokens (7 drafts + the
+# anchor) that see each other and the 4096 keys before them, at two context lengths (the cost
+# must not depend on the context); and a chunked prefill: a 2048-token prompt chunk appended to a
+# 129024-token context and attended causally (every token sees the context and the chunk's
+# earlier tokens).
+EXTENSIONS.update({
+    8: CaseSpec("draft sliding-window attention: 2 seqs x 32768, q8 non-causal block, window 4096, Hq24/Hkv4, "
+                "D256, E5M2 KV, page 2048",
+                contexts=(32768,) * 2, num_q_tokens=8, num_q_heads=24, num_kv_heads=4, head_dim=256,
+                page_size=2048, kv_dtype="e5m2", seed=1008, causal=False, window=4096),
+    9: CaseSpec("draft sliding-window attention: 2 seqs x 262144, q8 non-causal block, window 4096, Hq24/Hkv4, "
+                "D256, E5M2 KV, page 2048",
+                contexts=(262144,) * 2, num_q_tokens=8, num_q_heads=24, num_kv_heads=4, head_dim=256,
+                page_size=2048, kv_dtype="e5m2", seed=1009, causal=False, window=4096),
+    10: CaseSpec("chunked prefill: 1 seq, 2048-token chunk appended to 129024 cached tokens (keys up to 131072), "
+                 "causal, Hq24/Hkv4, D256, E4M3 KV, page 2048",
+                 contexts=(129024,), num_q_tokens=2048, num_q_heads=24, num_kv_heads=4, head_dim=256,
+                 page_size=2048, kv_dtype="e4m3", append_new=2048, seed=1010),
+})
 
 ALL = {**CONFIGS, **EXTENSIONS}
 

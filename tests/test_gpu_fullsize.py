@@ -1,6 +1,7 @@
 """The five benchmark workloads and the extension workloads (q16 verify, one scale per KV
-head) at full size, in the launch configuration the benchmark times (automatic split plan),
-checked against the oracle.
+head, the draft's non-causal sliding window at 32K and 256K keys, a 2048-token prefill chunk at
+128K keys) at full size, in the launch configuration the benchmark times (automatic split
+plan), checked against the oracle.
 
 * Cache bytes: every byte the append kernel wrote, over every token of the workload, compared
   chunk by chunk with the oracle's quantisation of the same fp16 inputs (read off a table of
@@ -19,11 +20,13 @@ import torch
 from paged_fp8_kv_cache_gb300 import binding as pf
 from paged_fp8_kv_cache_gb300 import workloads
 from tests.gpu_helpers import GpuCase
-from tests.oracle_helpers import expected_rows, head_tables, oracle_attention, unit_caches
+from oracle import attention
+from tests.oracle_helpers import expected_rows, head_tables, unit_caches
 
 pytestmark = pytest.mark.gpu
 
-UNITS_CHECKED = {1: None, 2: None, 3: None, 4: 3, 5: 64, 6: 3, 7: None}
+UNITS_CHECKED = {1: None, 2: None, 3: None, 4: 3, 5: 64, 6: 3, 7: None, 8: 4, 9: 3, 10: None}
+TOKENS_CHECKED = 24  # query tokens sampled per unit of a prefill chunk (the oracle's cost grows with rows x keys)
 CHUNK_TOKENS = 1 << 15
 
 
@@ -53,12 +56,12 @@ def check_every_cache_byte(g, case, tables):
             assert np.array_equal(got_v, want_v), f"V cache bytes differ in tokens {a}..{a + sl.size}"
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("cfg", sorted(workloads.ALL))
 def test_full_size_workload(cfg):
     case = workloads.make_case(workloads.ALL[cfg])
     s = case.spec
     g = GpuCase(case)
-    out, lse = g.decode()
+    out, lse = g.attention(causal=s.causal, window=s.window)
     torch.cuda.synchronize()
 
     tables = head_tables(case)
@@ -70,11 +73,19 @@ def test_full_size_workload(cfg):
     n = UNITS_CHECKED[cfg]
     units = all_units if n is None else [all_units[i] for i in rng.choice(len(all_units), n, replace=False)]
     kc, vc = unit_caches(case, units, tables)
-    o_ref, l_ref = oracle_attention(case, kc, vc, units=units)
     T, g_ = s.num_q_tokens, s.num_q_heads // s.num_kv_heads
+    tokens = None
+    if T > 16:  # a prefill chunk: slab boundaries, the ends and a seeded sample of its tokens
+        ts = 64 // g_
+        tokens = sorted(set([0, 1, ts - 1, ts, T - ts - 1, T - 1] +
+                            [int(t) for t in rng.choice(T, TOKENS_CHECKED, replace=False)]))
+    o_ref, l_ref = attention.paged_attention(case.q, kc, vc, case.block_table, case.seq_lens, T, s.num_kv_heads,
+                                             s.page_size, s.kv_dtype, case.k_scale, case.v_scale, case.softmax_scale,
+                                             units=units, causal=s.causal, window=s.window, tokens=tokens)
     rows = np.zeros(o_ref.shape[:2], bool)
     for b, kvh in units:
-        rows[b * T:(b + 1) * T, kvh * g_:(kvh + 1) * g_] = True
+        for t in (range(T) if tokens is None else tokens):
+            rows[b * T + t, kvh * g_:(kvh + 1) * g_] = True
     o = out.float().cpu().numpy().astype(np.float64)
     l = lse.cpu().numpy().astype(np.float64)
     # each query head's KV-head gain (1 without head gains)
