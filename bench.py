@@ -342,7 +342,11 @@ class DeviceWorkload:
 
 
 def time_steps(dw, torch, K, W, flush, e2e=False):
-    """Device time (ms) of K steps, L2 flushed before each; and decode-call times."""
+    """Device time (ms) of K steps, L2 flushed before each; and decode-call times. A step with an
+    append records a middle event before the decode call; without one the step is the decode call
+    and no extra event sits inside it."""
+    mid = dw.has_append and not e2e
+
     def step(ev=None):
         if e2e:
             dw.h2d()
@@ -358,12 +362,12 @@ def time_steps(dw, torch, K, W, flush, e2e=False):
         step()
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    mids = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(K)] if mid else starts
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     for i in range(K):
         flush()
         starts[i].record()
-        step(mids[i])
+        step(mids[i] if mid else None)
         ends[i].record()
     torch.cuda.synchronize()
     total = sum(s.elapsed_time(e) for s, e in zip(starts, ends))

@@ -82,18 +82,26 @@ struct VerifyShape {
   static constexpr int PT_BYTES = (KT / 64) * NMAX * 128;  // one P^T buffer (fp16, K-major, 64-key blocks)
   static constexpr int MT = D / 128;                     // O^T M-tiles
   static constexpr int TMEM_COLS = 512;
-  static constexpr int COL_S = 0;                        // NQ: S^T, one column group per Q term
-  static constexpr int COL_O = NQ;                       // MT x NMAX: O^T
+  // S^T accumulators: up to 48 rows the three Q terms are stacked along N (one MMA of N = 3 x
+  // rows per 32 head-dim elements; the softmax adds the three column groups); at 64 rows they
+  // accumulate into one group of NMAX columns (three MMAs of N = rows per 32 elements), which
+  // reads a third of the TMEM words per logit and leaves room for two V^T operands
+  static constexpr bool ONE_S = (NMAX == 64);
+  static constexpr int NS_COLS = ONE_S ? NMAX : NQ;
+  static constexpr int COL_S = 0;                        // NS_COLS: S^T
+  static constexpr int COL_O = NS_COLS;                  // MT x NMAX: O^T
   static constexpr int COL_AV = ((COL_O + MT * NMAX + 31) / 32) * 32;  // NAV x AV_COLS: V^T operands
   static constexpr int AV_COLS = MT * KT / 2;            // one V^T operand (fp16 pairs)
   static constexpr int NAV = COL_AV + 2 * AV_COLS <= TMEM_COLS ? 2 : 1;
   static_assert(COL_AV + NAV * AV_COLS <= TMEM_COLS, "TMEM budget");
-  // The V^T operands are written and consumed in 64-key halves: NHB half-buffers of HALF_COLS
-  // columns (M-tile mt of a half at column mt * KT / 4), so that even with room for a single
-  // 128-key operand (64 rows at D = 256) the converter writes one half while the O^T MMAs read
-  // the other.
-  static constexpr int HALF_COLS = MT * KT / 4;
-  static constexpr int NHB = 2 * NAV;
+  // The V^T operands are written and consumed in units of UK keys, in two buffers of UNIT_COLS
+  // columns (M-tile mt of a unit at column mt * UK / 2): whole 128-key tiles where two fit, 64-key
+  // halves where TMEM holds a single 128-key operand (64 rows at D = 256), so that the converter
+  // always writes one buffer while the O^T MMAs read the other.
+  static constexpr int UPT = NAV == 2 ? 1 : 2;  // conversion units per tile
+  static constexpr int UK = KT / UPT;           // keys per unit
+  static constexpr int UNIT_COLS = MT * UK / 2;
+  static constexpr int NHB = 2;                 // unit buffers
   static_assert(NQ <= 256, "MMA N");
   static_assert(HN % 8 == 0, "softmax rows come in TMEM loads of 8 columns");
   // misc: m_ref, alpha, sc2r, rscale, wred[4], lsum[4], m_use, thr, dx (NMAX floats each),
@@ -105,7 +113,7 @@ struct VerifyShape {
   static constexpr int NK = FIT / 2 > 4 ? 4 : FIT / 2;
   static constexpr int NV = FIT - NK > 4 ? 4 : FIT - NK;
   static_assert(NK >= 2 && NV >= 2, "shared memory budget");
-  static_assert(2 * NK + 2 * NV + 16 <= 32, "mbarrier slots");
+  static_assert(2 * NK + 2 * NV + 12 <= 32, "mbarrier slots");
   // shared memory map (offsets from the 1 KB-aligned base)
   static constexpr int OFF_KRING = 0;
   static constexpr int OFF_VRING = OFF_KRING + NK * KV_TILE;
@@ -286,9 +294,9 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
   uint64_t* kempty = kfull + NK;       // [NK] MMA commit: S^T MMAs done reading the K tile
   uint64_t* vfull = kempty + NK;       // [NV] producer -> V converter
   uint64_t* vempty = vfull + NV;       // [NV] V converter -> producer
-  uint64_t* av_full = vempty + NV;     // [NHB] V converter -> MMA (V^T half written)
-  uint64_t* av_free = av_full + 4;     // [NHB] MMA commit: O^T MMAs done with a V^T half
-  uint64_t* s_full = av_free + 4;      // MMA commit: S^T ready
+  uint64_t* av_full = vempty + NV;     // [NHB] V converter -> MMA (V^T unit written)
+  uint64_t* av_free = av_full + 2;     // [NHB] MMA commit: O^T MMAs done with a V^T unit
+  uint64_t* s_full = av_free + 2;      // MMA commit: S^T ready
   uint64_t* s_free = s_full + 1;       // softmax -> MMA: S^T read into registers
   uint64_t* pt_full = s_free + 1;      // [2] softmax -> MMA: P^T written
   uint64_t* pt_free = pt_full + 2;     // [2] MMA commit: O^T MMAs of the tile done (P^T buffer free)
@@ -497,7 +505,7 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && ntiles > 0) {
       constexpr int NHB = S::NHB;
-      const uint32_t idesc_qk = umma_idesc_f8(S::NQ, KV == kKvE4m3 ? 0u : 1u);
+      const uint32_t idesc_qk = umma_idesc_f8(S::NS_COLS, KV == kKvE4m3 ? 0u : 1u);
       const uint32_t idesc_pv = umma_idesc_f16(NMAX);
       // descriptors of the operands' first k-slices; a k-step adds its byte offset / 16 to the
       // start-address field (every operand lies below 256 KB, so the 14-bit field never carries)
@@ -521,7 +529,15 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
         for (int ks = 0; ks < D / 32; ++ks) {  // 32 FP8 dims = 32 bytes of a swizzled row per MMA
           const uint32_t koff = ((ks >> 2) * S::SUB + (ks & 3) * 32) >> 4;
           const uint32_t qoff = ((ks >> 2) * S::Q_BLK + (ks & 3) * 32) >> 4;
-          umma_ss_f8(tbase + S::COL_S, ka + koff, q_desc + qoff, idesc_qk, ks > 0 ? 1u : 0u);
+          if constexpr (S::ONE_S) {
+            // term t of every row is B row t * NMAX + r: its descriptor starts NMAX rows further
+#pragma unroll
+            for (int t = 0; t < kQTerms; ++t)
+              umma_ss_f8(tbase + S::COL_S, ka + koff, q_desc + qoff + static_cast<uint32_t>((t * NMAX * 128) >> 4),
+                         idesc_qk, (ks > 0 || t > 0) ? 1u : 0u);
+          } else {
+            umma_ss_f8(tbase + S::COL_S, ka + koff, q_desc + qoff, idesc_qk, ks > 0 ? 1u : 0u);
+          }
         }
         umma_commit(s_full);
         umma_commit(&kempty[sn % NK]);
@@ -538,11 +554,12 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
           issue_s(1);
         }
       }
+      constexpr int UPT = S::UPT;
       for (int on = 0; on < ntiles && ok; ++on) {
-        // conversion units 2*on (keys 0-63) and 2*on + 1 (keys 64-127) of tile on; each parity
-        // wait on a half-buffer is sound for the same reason as above (units u - NHB, u, u + NHB
-        // of a half-buffer are waited for in order)
-        ok = mbar_wait(&av_full[(2 * on) % NHB], ((2 * on) / NHB) & 1) && mbar_wait(&pt_full[on & 1], (on >> 1) & 1);
+        // conversion units UPT*on .. UPT*on + UPT-1 of tile on; each parity wait on a unit buffer
+        // is sound for the same reason as above (units u - NHB, u, u + NHB of a buffer are waited
+        // for in order)
+        ok = mbar_wait(&av_full[(UPT * on) % NHB], ((UPT * on) / NHB) & 1) && mbar_wait(&pt_full[on & 1], (on >> 1) & 1);
         if (!ok) break;
         const int sn = on + 2;
         if (sn < ntiles) {
@@ -554,21 +571,21 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
         tc_fence_after();
         const uint64_t pt = pt_desc + static_cast<uint64_t>(((on & 1) * S::PT_BYTES) >> 4);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int u = 2 * on + h;
-          if (h == 1) {
+        for (int h = 0; h < UPT; ++h) {
+          const int u = UPT * on + h;
+          if (h > 0) {
             ok = mbar_wait(&av_full[u % NHB], (u / NHB) & 1);
             if (!ok) break;
             tc_fence_after();
           }
-          const uint32_t av = tbase + S::COL_AV + (u % NHB) * S::HALF_COLS;
+          const uint32_t av = tbase + S::COL_AV + (u % NHB) * S::UNIT_COLS;
 #pragma unroll
-          for (int kh = 0; kh < KT / 32; ++kh) {
-            const int ks = 4 * h + kh;  // 16-key step of the tile
+          for (int kh = 0; kh < S::UK / 16; ++kh) {
+            const int ks = h * (S::UK / 16) + kh;  // 16-key step of the tile
             const uint32_t poff = ((ks >> 2) * NMAX * 128 + (ks & 3) * 32) >> 4;
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
-              umma_ts(tbase + S::COL_O + mt * NMAX, av + mt * (KT / 4) + 8 * kh, pt + poff, idesc_pv,
+              umma_ts(tbase + S::COL_O + mt * NMAX, av + mt * (S::UK / 2) + 8 * kh, pt + poff, idesc_pv,
                       (on > 0 || ks > 0) ? 1u : 0u);
           }
           umma_commit(&av_free[u % NHB]);
@@ -602,11 +619,11 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
       const int valid = min(KT, t1 - (t0 + it * KT));
       uint32_t av = 0;
       // a full tile and the range's last, partial one take separate copies of the loop, so that
-      // the full tiles carry no per-key range checks; keys k_lo .. k_lo + 63 go to one half-buffer
-      auto convert_half = [&](auto tail_tag, int k_lo) {
+      // the full tiles carry no per-key range checks; keys k_lo .. k_lo + UK - 1 go to one buffer
+      auto convert_unit = [&](auto tail_tag, int k_lo) {
         constexpr bool kTail = decltype(tail_tag)::value;
 #pragma unroll 1
-        for (int k0 = k_lo; k0 < k_lo + KT / 2; k0 += 32) {
+        for (int k0 = k_lo; k0 < k_lo + S::UK; k0 += 32) {
           const unsigned char* vrow = Vs + k0 * kBoxBytes;  // rows k0.. of the tile (k0 % 8 == 0)
           uint32_t v0[16], v1[16];
 #pragma unroll
@@ -637,23 +654,23 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
             }
           }
           tmem_st16(av + ((k0 - k_lo) >> 1), v0);
-          if constexpr (MT == 2) tmem_st16(av + KT / 4 + ((k0 - k_lo) >> 1), v1);
+          if constexpr (MT == 2) tmem_st16(av + S::UK / 2 + ((k0 - k_lo) >> 1), v1);
         }
       };
-      for (int h = 0; h < 2; ++h) {
-        const int u = 2 * it + h;  // conversion unit: half h of tile it
-        // half-buffer u % NHB is free once the O^T MMAs of unit u - NHB are done (sound: this
+      for (int h = 0; h < S::UPT; ++h) {
+        const int u = S::UPT * it + h;  // conversion unit h of tile it
+        // unit buffer u % NHB is free once the O^T MMAs of unit u - NHB are done (sound: this
         // thread saw that barrier's previous phase, of unit u - 2*NHB, before converting u - NHB)
         if (u >= S::NHB && !mbar_wait(&av_free[u % S::NHB], ((u / S::NHB) - 1) & 1)) {
           alive = false;
           break;
         }
         tc_fence_after();
-        av = tq + S::COL_AV + (u % S::NHB) * S::HALF_COLS;
+        av = tq + S::COL_AV + (u % S::NHB) * S::UNIT_COLS;
         if (valid < KT) {
-          convert_half(BoolTag<true>{}, h * (KT / 2));
+          convert_unit(BoolTag<true>{}, h * S::UK);
         } else {
-          convert_half(BoolTag<false>{}, h * (KT / 2));
+          convert_unit(BoolTag<false>{}, h * S::UK);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -745,8 +762,10 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
         float sc[8], mu[8], th[8];
         const uint32_t col = tq + S::COL_S + rbase + c;
         tmem_ld8(col, v0);
-        tmem_ld8(col + NMAX, v1);
-        tmem_ld8(col + 2 * NMAX, v2);
+        if constexpr (!S::ONE_S) {
+          tmem_ld8(col + NMAX, v1);
+          tmem_ld8(col + 2 * NMAX, v2);
+        }
         load8(sc2r + rbase + c, sc);
         load8(m_use + rbase + c, mu);
         load8(thr + rbase + c, th);
@@ -754,7 +773,8 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
         if (all_vis) {  // CTA-uniform: every row sees every key of the tile
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float raw = (__uint_as_float(v0[j]) + __uint_as_float(v1[j])) + __uint_as_float(v2[j]);
+            const float raw = S::ONE_S ? __uint_as_float(v0[j])
+                                       : (__uint_as_float(v0[j]) + __uint_as_float(v1[j])) + __uint_as_float(v2[j]);
             x[c + j] = fmaf(raw, sc[j], -mu[j]);
             exceed |= x[c + j] > th[j];
           }
@@ -763,7 +783,8 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
           for (int j = 0; j < 8; ++j) {
             const int r = rbase + c + j;
             const bool vis = r >= rmin && r < rmax;
-            const float raw = (__uint_as_float(v0[j]) + __uint_as_float(v1[j])) + __uint_as_float(v2[j]);
+            const float raw = S::ONE_S ? __uint_as_float(v0[j])
+                                       : (__uint_as_float(v0[j]) + __uint_as_float(v1[j])) + __uint_as_float(v2[j]);
             x[c + j] = vis ? fmaf(raw, sc[j], -mu[j]) : -CUDART_INF_F;
             exceed |= x[c + j] > th[j];
           }
