@@ -243,24 +243,20 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
       }
       ++n;
     };
-    // The pool is claimed in chunks of kClaimTiles tiles. The first claim is taken now, so that
-    // its latency overlaps the static tiles; each later one is taken as the previous chunk's
-    // first tile is issued, a chunk ahead of its use.
-    constexpr int kClaimTiles = 2;
-    const int nchunks = (npool + kClaimTiles - 1) / kClaimTiles;
+    // the first pool claim is taken now, so that its latency overlaps the static tiles; each
+    // later claim is taken as the previous claimed tile is issued
     int next_claim = 0;
-    if (nchunks > 0 && lane == 0) next_claim = atomicAdd(claim_ctr, 1);
+    if (npool > 0 && lane == 0) next_claim = atomicAdd(claim_ctr, 1);
     for (int it = 0; it < nstat && ok; ++it) issue_tile(tile0 + it * kTileKeys);
-    while (ok && nchunks > 0) {
+    while (ok && npool > 0) {
       const int c = __shfl_sync(0xffffffffu, next_claim, 0);
-      if (c >= nchunks) break;
+      if (c >= npool) break;
       if (lane == 0) next_claim = atomicAdd(claim_ctr, 1);
-      for (int k = c * kClaimTiles; k < min(npool, (c + 1) * kClaimTiles) && ok; ++k)
-        issue_tile(pool_base + k * kTileKeys);
+      issue_tile(pool_base + c * kTileKeys);
     }
     const int nreal = n;
     bool closed = false;
-    if (claim_ctr != nullptr && ok && (ok = acquire_slot())) {  // the end marker: a stage with no copy
+    if (ok && (ok = acquire_slot())) {  // the end marker: a stage with no copy
       if (lane == 0) {
         stage_key[n % NS] = -1;
         mbar_arrive(&full[n % NS]);
@@ -343,17 +339,14 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
   bool alive = true;
   const int groups_per_stage = kTileKeys / 16;
   for (int it = 0;; ++it) {
-    // static ranges: the CTA's own nstat tiles; claimed tiles: as the producer marked each
-    // stage, until its end marker
-    if (claim_ctr == nullptr && it >= nstat) break;
     const int s = it % NS;
     if (!mbar_wait(&full[s], (it / NS) & 1)) {
       if (lane == 0) atomicOr(p.err, kDevErrTimeout);
       alive = false;
       break;
     }
-    const int tile_start = claim_ctr == nullptr ? tile0 + it * kTileKeys : stage_key[s];
-    if (tile_start < 0) break;
+    const int tile_start = stage_key[s];
+    if (tile_start < 0) break;  // the producer's end marker
     const unsigned char* Ks = smem + s * S::STAGE;
     const unsigned char* Vs = Ks + S::KV_STAGE;
     const int valid = min(kTileKeys, kend - tile_start);

@@ -1,9 +1,9 @@
 """Run-time claiming of each unit's last tiles (decode kernel): when every CTA of a call is
 resident at once and the ranges are long, the CTAs of a (sequence, KV head) unit stream a static
-share of its first 7/8 tiles and then take its last 1/8 two tiles at a time from a counter in the
+share of its first 7/8 tiles and then take its last 1/8 one tile at a time from a counter in the
 workspace, which the call zeroes. Each CTA still writes one partial result, so the merge is the
 same. These tests check the results against the oracle, that the claiming really ran (every
-counter ends at the pool's chunks + participating CTAs), and that it does not depend on what the
+counter ends at pool tiles + participating CTAs), and that it does not depend on what the
 workspace held: garbage, a call with another batch in between, and CUDA-graph replays.
 """
 
@@ -41,7 +41,7 @@ def _lib(pflib):
 
 
 def expected_counts(case, splits):
-    """Final value of each unit's counter: its pool's chunks of two tiles plus the CTAs that took part."""
+    """Final value of each unit's counter: its pool tiles plus the CTAs that took part."""
     s = case.spec
     msl = int(case.seq_lens.max())
     S, C = pf.pfkv_decode_plan(case.B, s.num_q_tokens, s.num_q_heads, s.num_kv_heads, s.head_dim, s.page_size,
@@ -51,7 +51,7 @@ def expected_counts(case, splits):
         n = int(n)
         total = -(-n // TILE)
         parts = max(1, -(-n // C))
-        out.extend([-(-(total // 8) // 2) + parts] * s.num_kv_heads)  # claims of two tiles
+        out.extend([total // 8 + parts] * s.num_kv_heads)
     return np.array(out), S
 
 
