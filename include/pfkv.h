@@ -188,20 +188,11 @@ PFKV_API pfkv_status pfkv_decode_plan(int num_seqs, int num_q_tokens, int num_q_
  * num_q_heads:
  *   float o_part[rows][S][head_dim]   at offset 0
  *   float lse_part[rows][S]           right after it
- *   int   counters[num_seqs * slabs * num_kv_heads]  next, 16-byte aligned
  * Row index = (b * num_q_tokens + t) * num_q_heads + h. For a row whose
  * sequence was split, o_part[row][s] is the attention output of range s
  * normalised by its own weight sum and lse_part[row][s] its natural-log
  * LSE (-inf when the range holds no key visible to the row); rows of
- * sequences that were not split are not written. (With run-time tile
- * claiming, below, "range s" is the set of keys CTA s streamed: a static
- * share of the unit's first 7/8 tiles plus the tiles it claimed.)
- * The counters serve calls whose CTAs are all resident at once with long
- * ranges (the decode kernel, e.g. one long sequence): each CTA of a
- * (sequence, slab, KV head) unit then takes tiles of the unit's last 1/8
- * from its counter at run time, so that the unit's CTAs end together. The
- * call zeroes them itself (a memset on the caller's stream, part of a
- * captured graph like the kernels); the workspace needs no initialisation.
+ * sequences that were not split are not written.
  */
 PFKV_API size_t pfkv_decode_workspace_bytes(int num_seqs, int num_q_tokens, int num_q_heads,
                                    int num_kv_heads, int head_dim, int page_size,
@@ -337,10 +328,9 @@ PFKV_API size_t pfkv_attention_workspace_bytes(int num_seqs, int num_q_tokens, i
  *    (a call after cudaDeviceReset, in the device's new context, looks it up
  *    again); make that first call before any stream capture.
  *  - Sharing: every call on a device uses the same array, and it keeps the
- *    last call's contents (the call clears the tile counters it uses; nothing
- *    else in it needs to start at zero). Calls whose work overlaps on the GPU
- *    (other streams, or another thread's calls) race on it: order them on one
- *    stream or synchronise between them.
+ *    last call's contents (nothing in it needs to start at zero). Calls whose
+ *    work overlaps on the GPU (other streams, or another thread's calls)
+ *    race on it: order them on one stream or synchronise between them.
  */
 PFKV_API pfkv_status pfkv_paged_attention_decode_static_scratch(
     void* out, float* lse, const void* q, const void* k_cache, const void* v_cache,

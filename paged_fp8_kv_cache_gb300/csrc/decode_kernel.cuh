@@ -61,7 +61,7 @@ constexpr int decode_smem_bytes(int ncw) {
   const int obuf = ncw * 8 * NT * D * 4;
   const int ring = S::NS * S::STAGE;
   const int body = obuf > ring ? obuf : ring;
-  return body + ncw * 8 * NT * 8 /* m, l */ + 2 * S::NS * 8 /* barriers */ + 8 * S::NS /* stage tile starts */;
+  return body + ncw * 8 * NT * 8 /* m, l */ + 2 * S::NS * 8 /* barriers */;
 }
 
 template <int D, int KV, int NT>
@@ -108,39 +108,15 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
   const int nsplit_b = span_splits(sp, p.split_tokens);
   if (split >= nsplit_b) return;
   const int R = (sp.ts1 - sp.ts0) * p.G;  // query rows of this slab
-  const int kend = sp.hi >= sp.lo ? sp.hi + 1 : 0;  // keys past the slab's last visible one are never used
-  // The tiles this CTA streams: its range [t0, t1) -- or, when the call claims tiles at run time,
-  // its share of the first 7/8 of the slab's tiles (a static part) followed by tiles of the last
-  // 1/8 (the unit's pool) taken one at a time from a counter the call zeroed: CTAs that run
-  // fast take more of them, so the ranges of a unit end together. Either way the CTA's keys are
-  // one partial result in slot `split`.
-  int tile0, nstat, npool = 0, pool_base = 0;
-  int* claim_ctr = nullptr;
-  if (p.claim_ctr != nullptr) {
-    const int total = kend > sp.base ? (kend - sp.base + kTileKeys - 1) / kTileKeys : 0;
-    npool = total / 8;
-    const int stat = total - npool;
-    const int q = (stat + nsplit_b - 1) / nsplit_b;
-    const int a = min(stat, split * q);
-    tile0 = sp.base + a * kTileKeys;
-    nstat = min(stat, a + q) - a;
-    pool_base = sp.base + stat * kTileKeys;
-    claim_ctr = p.claim_ctr + (static_cast<size_t>(b) * p.num_slabs + slab) * p.num_kv_heads + kvh;
-  } else {
-    const int t0 = sp.base + split * p.split_tokens;
-    const int t1 = min(kend, t0 + p.split_tokens);
-    tile0 = t0;
-    nstat = t1 > t0 ? (t1 - t0 + kTileKeys - 1) / kTileKeys : 0;
-  }
-  const int pfirst0 = tile0 >> p.page_shift;
+  const int t0 = sp.base + split * p.split_tokens;
+  const int t1 = sp.hi >= sp.lo ? min(sp.hi + 1, t0 + p.split_tokens) : t0;
+  const int ntiles = t1 > t0 ? (t1 - t0 + kTileKeys - 1) / kTileKeys : 0;
+  const int pfirst0 = t0 >> p.page_shift;
 
-  const int body_bytes = decode_smem_bytes<D, KV, NT>(ncw) - ncw * ROWS_W * 8 - 2 * NS * 8 - 8 * NS;
+  const int body_bytes = decode_smem_bytes<D, KV, NT>(ncw) - ncw * ROWS_W * 8 - 2 * NS * 8;
   float2* ml_buf = reinterpret_cast<float2*>(smem + body_bytes);  // [ncw][ROWS_W] (m, l)
   uint64_t* full = reinterpret_cast<uint64_t*>(ml_buf + ncw * ROWS_W);
   uint64_t* empty = full + NS;
-  // key of each stage's first tile row, written by the producer before it arrives on the stage's
-  // full barrier (-1: no more tiles)
-  volatile int* stage_key = reinterpret_cast<volatile int*>(empty + NS);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -157,123 +133,101 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
     // The whole warp walks the tiles; its 32 lanes fetch 32 consecutive page
     // ids of the range at a time (one coalesced load instead of a chain of
     // dependent ones) and lane 0 issues the copies, reading ids by shuffle.
-    if (lane == 0) {
-      prefetch_tensormap(&tmk);
-      prefetch_tensormap(&tmv);
-    }
-    const int P = p.page_size;
-    const int* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks;
-    const int page_last = (kend - 1) >> p.page_shift;  // -1 when there are no keys
-    // The lanes hold the ids of pages chunk_base .. chunk_base + 31 (the first chunk was
-    // fetched above when it did not depend on the length), and the raw ids of the next 32
-    // pages, loaded one chunk ahead: moving to the next chunk never waits on the table (with
-    // 16-token pages a chunk lasts 8 tiles). An id outside the pool is flagged when its chunk
-    // becomes current and block 0 is read instead.
-    auto load_raw = [&](int first) -> int {
-      const int mine = first + lane;
-      return mine <= page_last ? bt[mine] : 0;
-    };
-    auto checked = [&](int raw, int first) -> int {
-      if (first + lane > page_last) return 0;
-      if (static_cast<unsigned>(raw) >= static_cast<unsigned>(p.num_blocks)) {
-        atomicOr(p.err, kDevErrBlockId);
-        return 0;
+    if (ntiles > 0) {
+      if (lane == 0) {
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
       }
-      return raw;
-    };
-    int chunk_base = pfirst0;
-    int my_id = checked(pguess == pfirst0 ? pre_id : load_raw(pfirst0), pfirst0);
-    int next_raw = load_raw(pfirst0 + 32);
-    auto page_id = [&](int pidx) -> int {
-      if (pidx < chunk_base || pidx >= chunk_base + 32) {
-        my_id = pidx == chunk_base + 32 ? checked(next_raw, pidx) : checked(load_raw(pidx), pidx);
-        chunk_base = pidx;
-        next_raw = load_raw(chunk_base + 32);
-      }
-      return __shfl_sync(0xffffffffu, my_id, pidx - chunk_base);
-    };
-    bool ok = true;
-    int n = 0;  // stages filled so far
-    // stage n's slot, once the consumers released its previous contents (sound: this warp
-    // waited for that barrier's previous phase, of stage n - 2*NS, before filling stage n - NS)
-    auto acquire_slot = [&]() -> bool {
-      bool got = true;
-      if (n >= NS) {
-        if (lane == 0) got = mbar_wait(&empty[n % NS], ((n / NS) - 1) & 1);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got && lane == 0) atomicOr(p.err, kDevErrTimeout);
-      }
-      return got;
-    };
-    auto issue_tile = [&](int tile_start) {
-      if (!(ok = acquire_slot())) return;
-      const int s = n % NS;
-      unsigned char* kdst = smem + s * S::STAGE;
-      unsigned char* vdst = kdst + S::KV_STAGE;
-      if (lane == 0) stage_key[s] = tile_start;
-      if (P >= kTileKeys) {
-        const int blk = page_id(tile_start >> p.page_shift);
-        const int row = (blk * p.num_kv_heads + kvh) * P + (tile_start & (P - 1));
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[s], 2 * S::KV_STAGE);
-#pragma unroll
-          for (int bx = 0; bx < NBOX; ++bx) {
-            tma_load_2d(kdst + bx * kSubTileBytes, &tmk, &full[s], bx * (kBoxBytes / ELT), row);
-            tma_load_2d(vdst + bx * kSubTileBytes, &tmv, &full[s], bx * (kBoxBytes / ELT), row);
+      const int P = p.page_size;
+      const int* bt = p.block_table + static_cast<size_t>(b) * p.max_blocks;
+      const int page_last = (t1 - 1) >> p.page_shift;
+      // The lanes hold the ids of pages chunk_base .. chunk_base + 31 (the first chunk was
+      // fetched above when it did not depend on the length), and the raw ids of the next 32
+      // pages, loaded one chunk ahead: moving to the next chunk never waits on the table (with
+      // 16-token pages a chunk lasts 8 tiles). An id outside the pool is flagged when its chunk
+      // becomes current and block 0 is read instead.
+      auto load_raw = [&](int first) -> int {
+        const int mine = first + lane;
+        return mine <= page_last ? bt[mine] : 0;
+      };
+      auto checked = [&](int raw, int first) -> int {
+        if (first + lane > page_last) return 0;
+        if (static_cast<unsigned>(raw) >= static_cast<unsigned>(p.num_blocks)) {
+          atomicOr(p.err, kDevErrBlockId);
+          return 0;
+        }
+        return raw;
+      };
+      int chunk_base = pfirst0;
+      int my_id = checked(pguess == pfirst0 ? pre_id : load_raw(pfirst0), pfirst0);
+      int next_raw = load_raw(pfirst0 + 32);
+      auto page_id = [&](int pidx) -> int {
+        if (pidx < chunk_base || pidx >= chunk_base + 32) {
+          my_id = pidx == chunk_base + 32 ? checked(next_raw, pidx) : checked(load_raw(pidx), pidx);
+          chunk_base = pidx;
+          next_raw = load_raw(chunk_base + 32);
+        }
+        return __shfl_sync(0xffffffffu, my_id, pidx - chunk_base);
+      };
+      bool ok = true;
+      for (int it = 0; it < ntiles && ok; ++it) {
+        const int s = it % NS;
+        if (it >= NS) {
+          bool got = true;
+          if (lane == 0) got = mbar_wait(&empty[s], ((it / NS) - 1) & 1);
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) {
+            if (lane == 0) atomicOr(p.err, kDevErrTimeout);
+            ok = false;
+            break;
           }
         }
-      } else {
-        const int valid = min(kTileKeys, kend - tile_start);
-        const int npages = (valid + P - 1) >> p.page_shift;
-        const int pfirst = tile_start >> p.page_shift;
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], 2 * NBOX * npages * P * kBoxBytes);
-        for (int pg = 0; pg < npages; ++pg) {
-          const int blk = page_id(pfirst + pg);
-          const int row = (blk * p.num_kv_heads + kvh) * P;
+        unsigned char* kdst = smem + s * S::STAGE;
+        unsigned char* vdst = kdst + S::KV_STAGE;
+        const int tile_start = t0 + it * kTileKeys;
+        if (P >= kTileKeys) {
+          const int blk = page_id(tile_start >> p.page_shift);
+          const int row = (blk * p.num_kv_heads + kvh) * P + (tile_start & (P - 1));
           if (lane == 0) {
+            mbar_arrive_expect_tx(&full[s], 2 * S::KV_STAGE);
 #pragma unroll
             for (int bx = 0; bx < NBOX; ++bx) {
-              tma_load_2d(kdst + bx * kSubTileBytes + pg * P * kBoxBytes, &tmk, &full[s], bx * (kBoxBytes / ELT),
-                          row);
-              tma_load_2d(vdst + bx * kSubTileBytes + pg * P * kBoxBytes, &tmv, &full[s], bx * (kBoxBytes / ELT),
-                          row);
+              tma_load_2d(kdst + bx * kSubTileBytes, &tmk, &full[s], bx * (kBoxBytes / ELT), row);
+              tma_load_2d(vdst + bx * kSubTileBytes, &tmv, &full[s], bx * (kBoxBytes / ELT), row);
+            }
+          }
+        } else {
+          const int valid = min(kTileKeys, t1 - tile_start);
+          const int npages = (valid + P - 1) >> p.page_shift;
+          const int pfirst = tile_start >> p.page_shift;
+          if (lane == 0) mbar_arrive_expect_tx(&full[s], 2 * NBOX * npages * P * kBoxBytes);
+          for (int pg = 0; pg < npages; ++pg) {
+            const int blk = page_id(pfirst + pg);
+            const int row = (blk * p.num_kv_heads + kvh) * P;
+            if (lane == 0) {
+#pragma unroll
+              for (int bx = 0; bx < NBOX; ++bx) {
+                tma_load_2d(kdst + bx * kSubTileBytes + pg * P * kBoxBytes, &tmk, &full[s], bx * (kBoxBytes / ELT),
+                            row);
+                tma_load_2d(vdst + bx * kSubTileBytes + pg * P * kBoxBytes, &tmv, &full[s], bx * (kBoxBytes / ELT),
+                            row);
+              }
             }
           }
         }
       }
-      ++n;
-    };
-    // the first pool claim is taken now, so that its latency overlaps the static tiles; each
-    // later claim is taken as the previous claimed tile is issued
-    int next_claim = 0;
-    if (npool > 0 && lane == 0) next_claim = atomicAdd(claim_ctr, 1);
-    for (int it = 0; it < nstat && ok; ++it) issue_tile(tile0 + it * kTileKeys);
-    while (ok && npool > 0) {
-      const int c = __shfl_sync(0xffffffffu, next_claim, 0);
-      if (c >= npool) break;
-      if (lane == 0) next_claim = atomicAdd(claim_ctr, 1);
-      issue_tile(pool_base + c * kTileKeys);
-    }
-    const int nreal = n;
-    bool closed = false;
-    if (ok && (ok = acquire_slot())) {  // the end marker: a stage with no copy
+      // do not leave while copies may still land in this CTA's shared memory
       if (lane == 0) {
-        stage_key[n % NS] = -1;
-        mbar_arrive(&full[n % NS]);
-      }
-      closed = true;
-    }
-    // Do not leave while copies may still land in this CTA's shared memory. The end marker took
-    // the slot of tile nreal - NS, which the consumers had released (its copy landed).
-    if (lane == 0) {
-      for (int it = max(0, nreal - NS + (closed ? 1 : 0)); it < nreal; ++it) {
-        if (!mbar_wait(&full[it % NS], (it / NS) & 1)) {
-          atomicOr(p.err, kDevErrTimeout);
-          break;
+        const int first_pending = max(0, ntiles - NS);
+        for (int it = first_pending; it < ntiles; ++it) {
+          if (!mbar_wait(&full[it % NS], (it / NS) & 1)) {
+            atomicOr(p.err, kDevErrTimeout);
+            break;
+          }
         }
       }
+      __syncwarp();
     }
-    __syncwarp();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     return;
   }
@@ -313,12 +267,27 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
     }
   }
 
-  // Keys every row of the slab sees: [max_lo, min_hi] (the bounds grow with the query token, so
-  // they are its first token's upper and last token's lower bound). Groups inside it need no
-  // masking; elsewhere each row's own bounds follow from its query token (padding rows past R
-  // take the slab's last token: they are never written out).
-  const int min_hi = key_hi(N, p.T, sp.ts0, p.causal);
-  const int max_lo = key_lo(N, p.T, sp.ts1 - 1, p.window);
+  // query token of the two rows (2c, 2c+1) of every n-tile this lane accumulates; the rows'
+  // visible keys [key_lo, key_hi] follow from it where a group needs masking (padding rows past
+  // R take the slab's last token: they are never written out)
+  int rtok[NT][2];
+  int min_hi = INT_MAX, max_lo = 0;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int row = row_base + nt * 8 + 2 * c + e;
+      rtok[nt][e] = row < R ? sp.ts0 + row / p.G : sp.ts1 - 1;
+      if (row < R) {
+        min_hi = min(min_hi, key_hi(N, p.T, rtok[nt][e], p.causal));
+        max_lo = max(max_lo, key_lo(N, p.T, rtok[nt][e], p.window));
+      }
+    }
+#pragma unroll
+  for (int off = 1; off < 4; off <<= 1) {
+    min_hi = min(min_hi, __shfl_xor_sync(0xffffffffu, min_hi, off));
+    max_lo = max(max_lo, __shfl_xor_sync(0xffffffffu, max_lo, off));
+  }
 
   float o[MTILES][NT][4];
 #pragma unroll
@@ -338,18 +307,17 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
 
   bool alive = true;
   const int groups_per_stage = kTileKeys / 16;
-  for (int it = 0;; ++it) {
+  for (int it = 0; it < ntiles; ++it) {
     const int s = it % NS;
     if (!mbar_wait(&full[s], (it / NS) & 1)) {
       if (lane == 0) atomicOr(p.err, kDevErrTimeout);
       alive = false;
       break;
     }
-    const int tile_start = stage_key[s];
-    if (tile_start < 0) break;  // the producer's end marker
     const unsigned char* Ks = smem + s * S::STAGE;
     const unsigned char* Vs = Ks + S::KV_STAGE;
-    const int valid = min(kTileKeys, kend - tile_start);
+    const int tile_start = t0 + it * kTileKeys;
+    const int valid = min(kTileKeys, t1 - tile_start);
 
     for (int grp = ts; grp < groups_per_stage; grp += p.nts) {
       if (grp * 16 >= valid) break;
@@ -427,10 +395,8 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
         for (int e = 0; e < 2; ++e) {
           float sa = sacc[nt][e] * sc2, sb = sacc[nt][2 + e] * sc2;
           if (need_mask) {
-            const int row = row_base + nt * 8 + 2 * c + e;
-            const int tok = row < R ? sp.ts0 + row / p.G : sp.ts1 - 1;
-            const int khi = key_hi(N, p.T, tok, p.causal);
-            const int klo = key_lo(N, p.T, tok, p.window);
+            const int khi = key_hi(N, p.T, rtok[nt][e], p.causal);
+            const int klo = key_lo(N, p.T, rtok[nt][e], p.window);
             if (keyA > khi || keyA < klo) sa = -CUDART_INF_F;
             if (keyB > khi || keyB < klo) sb = -CUDART_INF_F;
           }

@@ -323,23 +323,12 @@ pfkv_status make_plan(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_k
   return PFKV_OK;
 }
 
-// Workspace of a split plan: the partials, then (16-byte aligned) one int tile counter per
-// (sequence, slab, KV head), used when the decode kernel claims the tiles at the end of each unit
-// at run time (the call zeroes them).
-size_t counters_offset(const Plan& pl, int num_seqs, int T, int Hq, int D) {
+size_t workspace_for(const Plan& pl, int num_seqs, int T, int Hq, int D) {
+  if (pl.splits <= 1) return 0;
   const size_t rows = static_cast<size_t>(num_seqs) * T * Hq;
   const size_t o = rows * pl.splits * D * sizeof(float);
   const size_t l = rows * pl.splits * sizeof(float);
-  return (o + l + 15) & ~static_cast<size_t>(15);
-}
-
-size_t num_units(const Plan& pl, int num_seqs, int Hkv) {
-  return static_cast<size_t>(num_seqs) * pl.num_slabs * Hkv;
-}
-
-size_t workspace_for(const Plan& pl, int num_seqs, int T, int Hq, int Hkv, int D) {
-  if (pl.splits <= 1) return 0;
-  return counters_offset(pl, num_seqs, T, Hq, D) + num_units(pl, num_seqs, Hkv) * sizeof(int);
+  return o + l;
 }
 
 // The decode entry points keep their contract: causal, no window, 1..16 query tokens whose rows
@@ -377,7 +366,7 @@ size_t workspace_impl(int num_seqs, int num_q_tokens, int num_q_heads, int num_k
   if (make_plan(num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim, page_size, dtype, mask, window,
                 max_seq_len, num_splits_request, &pl) != PFKV_OK)
     return 0;
-  return workspace_for(pl, num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim);
+  return workspace_for(pl, num_seqs, num_q_tokens, num_q_heads, head_dim);
 }
 
 pfkv_status attention_impl(void* out, float* lse, const void* q, const void* k_cache, const void* v_cache,
@@ -409,18 +398,17 @@ pfkv_status attention_impl(void* out, float* lse, const void* q, const void* k_c
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 7)
     return fail(PFKV_ERR_INVALID_ARG, "q and out must be 8-byte aligned");
   if (reinterpret_cast<uintptr_t>(lse) & 3) return fail(PFKV_ERR_INVALID_ARG, "lse must be 4-byte aligned");
-  const size_t need = workspace_for(pl, num_seqs, num_q_tokens, num_q_heads, num_kv_heads, head_dim);
+  const size_t need = workspace_for(pl, num_seqs, num_q_tokens, num_q_heads, head_dim);
   if (need > 0) {
     if (!workspace || workspace_bytes < need)
       return fail(PFKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
     if (reinterpret_cast<uintptr_t>(workspace) & 15)
       return fail(PFKV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   }
-  int dev, sms;
+  int dev;
   unsigned* err;
   cudaError_t e = current_device(&dev);
   if (e == cudaSuccess) e = err_word(dev, &err);
-  if (e == cudaSuccess) e = sm_count(dev, &sms);
   if (e != cudaSuccess) return cuda_fail(e, "device set-up");
 
   CUtensorMap tmk, tmv;
@@ -462,21 +450,8 @@ pfkv_status attention_impl(void* out, float* lse, const void* q, const void* k_c
   p.window = pl.window;
   p.slab_tokens = pl.slab_tokens;
   p.num_slabs = pl.num_slabs;
-  p.claim_ctr = nullptr;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // Run-time claiming of each unit's last tiles (decode kernel), when every CTA of the call is
-  // resident at once (one wave) and the ranges are long: the CTAs of a unit then end together
-  // instead of over the spread of per-SM speeds. The counters start at zero on every call.
-  const size_t units = num_units(pl, num_seqs, num_kv_heads);
-  if (!pl.tc && pl.splits >= 4 && pl.split_tokens / pl.tile >= 16 &&
-      static_cast<long long>(units) * pl.splits <=
-          static_cast<long long>(sms) * ctas_per_sm(dev, pl.cfg, pl.ncw, false, 0)) {
-    unsigned char* ws = static_cast<unsigned char*>(workspace);
-    p.claim_ctr = reinterpret_cast<int*>(ws + counters_offset(pl, num_seqs, num_q_tokens, num_q_heads, head_dim));
-    e = cudaMemsetAsync(p.claim_ctr, 0, units * sizeof(int), s);
-    if (e != cudaSuccess) return cuda_fail(e, "clear tile counters");
-  }
   dim3 grid(pl.splits, num_kv_heads * pl.num_slabs, num_seqs);
   if (pl.tc) {
     e = kv == kKvE4m3 ? launch_verify_e4m3(head_dim, pl.nmax, tmk, tmv, p, grid, s, nullptr)

@@ -50,9 +50,6 @@ struct DecodeParams {
   int window;       // > 0: query t sees no key W or more positions before its own (0: no window)
   int slab_tokens;  // query tokens per CTA
   int num_slabs;    // ceil(T / slab_tokens)
-  // decode kernel: one tile counter per (sequence, slab, KV head), zeroed by the call, when the
-  // tiles at the end of each unit are claimed at run time; null: every CTA streams its own range
-  int* claim_ctr;
 };
 
 struct DecodeLaunch {
