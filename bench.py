@@ -59,8 +59,8 @@ L2_FLUSH_BYTES = 256 << 20  # > 2x the 129 MB L2
 FALLBACK_HBM_GBS = 6800.0
 # sources of each kernel (the hash ties a committed ncu summary to the code it measured)
 KERNEL_SOURCES = {
-    "decode_kernel": ["decode_kernel.cuh", "device_utils.cuh", "frag_layout.h"],
-    "verify_kernel": ["verify_kernel.cuh", "device_utils.cuh", "frag_layout.h", "verify_layout.h"],
+    "decode_kernel": ["decode_kernel.cuh", "device_utils.cuh", "frag_layout.h", "mask_span.h"],
+    "verify_kernel": ["verify_kernel.cuh", "device_utils.cuh", "frag_layout.h", "verify_layout.h", "mask_span.h"],
 }
 
 

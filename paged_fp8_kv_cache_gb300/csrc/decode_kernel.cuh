@@ -267,27 +267,12 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
     }
   }
 
-  // query token of the two rows (2c, 2c+1) of every n-tile this lane accumulates; the rows'
-  // visible keys [key_lo, key_hi] follow from it where a group needs masking (padding rows past
-  // R take the slab's last token: they are never written out)
-  int rtok[NT][2];
-  int min_hi = INT_MAX, max_lo = 0;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int row = row_base + nt * 8 + 2 * c + e;
-      rtok[nt][e] = row < R ? sp.ts0 + row / p.G : sp.ts1 - 1;
-      if (row < R) {
-        min_hi = min(min_hi, key_hi(N, p.T, rtok[nt][e], p.causal));
-        max_lo = max(max_lo, key_lo(N, p.T, rtok[nt][e], p.window));
-      }
-    }
-#pragma unroll
-  for (int off = 1; off < 4; off <<= 1) {
-    min_hi = min(min_hi, __shfl_xor_sync(0xffffffffu, min_hi, off));
-    max_lo = max(max_lo, __shfl_xor_sync(0xffffffffu, max_lo, off));
-  }
+  // Keys every row of the slab sees: [max_lo, min_hi] (the bounds grow with the query token, so
+  // they are its first token's upper and last token's lower bound). Groups inside it need no
+  // masking; elsewhere each row's own bounds follow from its query token (padding rows past R
+  // take the slab's last token: they are never written out).
+  const int min_hi = key_hi(N, p.T, sp.ts0, p.causal);
+  const int max_lo = key_lo(N, p.T, sp.ts1 - 1, p.window);
 
   float o[MTILES][NT][4];
 #pragma unroll
@@ -395,8 +380,10 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
         for (int e = 0; e < 2; ++e) {
           float sa = sacc[nt][e] * sc2, sb = sacc[nt][2 + e] * sc2;
           if (need_mask) {
-            const int khi = key_hi(N, p.T, rtok[nt][e], p.causal);
-            const int klo = key_lo(N, p.T, rtok[nt][e], p.window);
+            const int row = row_base + nt * 8 + 2 * c + e;
+            const int tok = row < R ? sp.ts0 + row / p.G : sp.ts1 - 1;
+            const int khi = key_hi(N, p.T, tok, p.causal);
+            const int klo = key_lo(N, p.T, tok, p.window);
             if (keyA > khi || keyA < klo) sa = -CUDART_INF_F;
             if (keyB > khi || keyB < klo) sb = -CUDART_INF_F;
           }
