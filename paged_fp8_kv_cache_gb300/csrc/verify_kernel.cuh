@@ -52,8 +52,6 @@
 #include <math_constants.h>
 #include <stdint.h>
 
-#include <type_traits>
-
 #include "device_utils.cuh"
 #include "frag_layout.h"
 #include "mask_span.h"
@@ -259,35 +257,8 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
   const int kvh = blockIdx.y % p.num_kv_heads;
   const int slab = p.num_slabs - 1 - static_cast<int>(blockIdx.y) / p.num_kv_heads;  // longest slabs first
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tid = threadIdx.x;
-
   // launched with programmatic stream serialisation: wait for the preceding grid first
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // The slab's query rows do not depend on the sequence length: warps 1-13 (which prepare Q while
-  // warp 0 starts the copies) issue the loads of all their rows now, together with the length
-  // and the scales, so that the prologue costs one memory round trip instead of one per row.
-  constexpr int PER_LANE = D / 32;             // 8 (D = 256) or 4 (D = 128) consecutive dims per lane
-  constexpr int NQW = kVerifyWarps - 1;        // warps preparing Q
-  constexpr int RPW = (NMAX + NQW - 1) / NQW;  // rows per such warp
-  using QVec = std::conditional_t<PER_LANE == 8, uint4, uint2>;
-  QVec qraw[RPW];
-  {
-    const int ts0 = slab * p.slab_tokens;
-    const int rows = (min(p.T, ts0 + p.slab_tokens) - ts0) * p.G;
-#pragma unroll
-    for (int i = 0; i < RPW; ++i) {
-      const int r = (warp - 1) + i * NQW;
-      qraw[i] = QVec{};
-      if (warp >= 1 && r < rows) {
-        const int tl = r / p.G, j = r - tl * p.G;
-        qraw[i] = *reinterpret_cast<const QVec*>(
-            p.q + ((static_cast<size_t>(b) * p.T + ts0 + tl) * p.num_q_heads + kvh * p.G + j) * D + lane * PER_LANE);
-      }
-    }
-  }
-  // the pool's scale, or this KV head's
-  const float kscale = p.k_scale[kvh * p.scale_stride], vscale = p.v_scale[kvh * p.scale_stride];
   int N = p.seq_lens[b];
   {
     const int cap = min(p.max_seq_len, p.max_blocks * p.page_size);
@@ -332,6 +303,9 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
   uint64_t* swg_bar = pt_free + 2;     // softmax warps' rendezvous (bounded waits, unlike bar.sync)
   uint64_t* tmem_done = swg_bar + 1;   // softmax warps -> MMA warp: last TMEM read done
 
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+
   if (tid == 0) {
     for (int s = 0; s < NK; ++s) {
       mbar_init(&kfull[s], 1);
@@ -360,24 +334,21 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
                  "r"(S::TMEM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  tc_fence_before();
-  __syncthreads();  // the barriers exist (warp 0 starts the copies now) and the TMEM slot is written
-  tc_fence_after();
+  // the pool's scale, or this KV head's
+  const float kscale = p.k_scale[kvh * p.scale_stride], vscale = p.v_scale[kvh * p.scale_stride];
   const float sc2 = p.softmax_scale * kscale * 1.4426950408889634f;
-  uint32_t tbase = 0;
-  bool alive = true;
-  // Q -> three E4M3 terms in shared memory (K-major, 128B swizzle), one warp per row; padded rows
-  // zero. Warps 1-13 meet on a named barrier afterwards; warp 0 is already copying.
-  if (warp >= 1) {
-#pragma unroll
-    for (int i = 0; i < RPW; ++i) {
-      const int r = (warp - 1) + i * NQW;
-      if (r >= NMAX) break;
+  // Q -> three E4M3 terms in shared memory (K-major, 128B swizzle), one warp per row; padded rows zero
+  {
+    constexpr int PER_LANE = D / 32;  // 8 (D = 256) or 4 (D = 128) consecutive dims per lane
+    for (int r = warp; r < NMAX; r += kVerifyWarps) {
       float x[PER_LANE];
       float mx = 0.f;
       if (r < R) {
+        const int tl = r / p.G, j = r - tl * p.G;
+        const __half* src =
+            p.q + ((static_cast<size_t>(b) * p.T + sp.ts0 + tl) * p.num_q_heads + kvh * p.G + j) * D + lane * PER_LANE;
         if constexpr (PER_LANE == 8) {
-          const uint4 v = qraw[i];
+          const uint4 v = *reinterpret_cast<const uint4*>(src);
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -386,7 +357,7 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
             x[2 * i + 1] = f.y;
           }
         } else {
-          const uint2 v = qraw[i];
+          const uint2 v = *reinterpret_cast<const uint2*>(src);
           const uint32_t w[2] = {v.x, v.y};
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
@@ -429,18 +400,19 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
         }
       }
     }
-    for (int i = tid - 32; i < NMAX; i += NQW * 32) {
+    for (int i = tid; i < NMAX; i += blockDim.x) {
       m_ref[i] = kNoRef;
       m_use[i] = 0.f;
       thr[i] = -CUDART_INF_F;
     }
-    if (tid == 32) flag[0] = flag[1] = flag[2] = 0;
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    tc_fence_before();
-    asm volatile("bar.sync 1, %0;" ::"r"(NQW * 32) : "memory");
-    tc_fence_after();
-    tbase = *tslot;
+    if (tid == 0) flag[0] = flag[1] = flag[2] = 0;
   }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  bool alive = true;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producers (lanes 0 and 1)
