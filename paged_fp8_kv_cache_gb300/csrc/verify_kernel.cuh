@@ -83,11 +83,11 @@ struct VerifyShape {
   static constexpr int MT = D / 128;                     // O^T M-tiles
   static constexpr int TMEM_COLS = 512;
   // S^T accumulators: up to 48 rows the three Q terms are stacked along N (one MMA of N = 3 x
-  // rows per 32 head-dim elements; the softmax adds the three column groups); at 64 rows they
-  // accumulate into one group of NMAX columns (three MMAs of N = rows per 32 elements), which
-  // reads a third of the TMEM words per logit and leaves room for two V^T operands
-  static constexpr bool ONE_S = (NMAX == 64);
-  static constexpr int NS_COLS = ONE_S ? NMAX : NQ;
+  // rows per 32 head-dim elements; the softmax adds the three column groups); at 64 rows terms 0
+  // and 1 are stacked (one MMA of N = 2 x rows) and term 2 accumulates onto term 1's columns (one
+  // MMA of N = rows): two column groups, which leave room for two V^T operands
+  static constexpr bool TWO_S = (NMAX == 64);
+  static constexpr int NS_COLS = TWO_S ? 2 * NMAX : NQ;
   static constexpr int COL_S = 0;                        // NS_COLS: S^T
   static constexpr int COL_O = NS_COLS;                  // MT x NMAX: O^T
   static constexpr int COL_AV = ((COL_O + MT * NMAX + 31) / 32) * 32;  // NAV x AV_COLS: V^T operands
@@ -506,6 +506,7 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
     if (lane == 0 && ntiles > 0) {
       constexpr int NHB = S::NHB;
       const uint32_t idesc_qk = umma_idesc_f8(S::NS_COLS, KV == kKvE4m3 ? 0u : 1u);
+      const uint32_t idesc_qk1 = umma_idesc_f8(NMAX, KV == kKvE4m3 ? 0u : 1u);  // term 2 alone (64 rows)
       const uint32_t idesc_pv = umma_idesc_f16(NMAX);
       // descriptors of the operands' first k-slices; a k-step adds its byte offset / 16 to the
       // start-address field (every operand lies below 256 KB, so the 14-bit field never carries)
@@ -529,14 +530,11 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
         for (int ks = 0; ks < D / 32; ++ks) {  // 32 FP8 dims = 32 bytes of a swizzled row per MMA
           const uint32_t koff = ((ks >> 2) * S::SUB + (ks & 3) * 32) >> 4;
           const uint32_t qoff = ((ks >> 2) * S::Q_BLK + (ks & 3) * 32) >> 4;
-          if constexpr (S::ONE_S) {
-            // term t of every row is B row t * NMAX + r: its descriptor starts NMAX rows further
-#pragma unroll
-            for (int t = 0; t < kQTerms; ++t)
-              umma_ss_f8(tbase + S::COL_S, ka + koff, q_desc + qoff + static_cast<uint32_t>((t * NMAX * 128) >> 4),
-                         idesc_qk, (ks > 0 || t > 0) ? 1u : 0u);
-          } else {
-            umma_ss_f8(tbase + S::COL_S, ka + koff, q_desc + qoff, idesc_qk, ks > 0 ? 1u : 0u);
+          umma_ss_f8(tbase + S::COL_S, ka + koff, q_desc + qoff, idesc_qk, ks > 0 ? 1u : 0u);
+          if constexpr (S::TWO_S) {
+            // term 2 of every row (B rows 2 * NMAX + r) onto term 1's columns
+            umma_ss_f8(tbase + S::COL_S + NMAX, ka + koff, q_desc + qoff + static_cast<uint32_t>((2 * NMAX * 128) >> 4),
+                       idesc_qk1, 1u);
           }
         }
         umma_commit(s_full);
@@ -762,10 +760,8 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
         float sc[8], mu[8], th[8];
         const uint32_t col = tq + S::COL_S + rbase + c;
         tmem_ld8(col, v0);
-        if constexpr (!S::ONE_S) {
-          tmem_ld8(col + NMAX, v1);
-          tmem_ld8(col + 2 * NMAX, v2);
-        }
+        tmem_ld8(col + NMAX, v1);
+        if constexpr (!S::TWO_S) tmem_ld8(col + 2 * NMAX, v2);
         load8(sc2r + rbase + c, sc);
         load8(m_use + rbase + c, mu);
         load8(thr + rbase + c, th);
@@ -773,7 +769,7 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
         if (all_vis) {  // CTA-uniform: every row sees every key of the tile
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float raw = S::ONE_S ? __uint_as_float(v0[j])
+            const float raw = S::TWO_S ? __uint_as_float(v0[j]) + __uint_as_float(v1[j])
                                        : (__uint_as_float(v0[j]) + __uint_as_float(v1[j])) + __uint_as_float(v2[j]);
             x[c + j] = fmaf(raw, sc[j], -mu[j]);
             exceed |= x[c + j] > th[j];
@@ -783,7 +779,7 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
           for (int j = 0; j < 8; ++j) {
             const int r = rbase + c + j;
             const bool vis = r >= rmin && r < rmax;
-            const float raw = S::ONE_S ? __uint_as_float(v0[j])
+            const float raw = S::TWO_S ? __uint_as_float(v0[j]) + __uint_as_float(v1[j])
                                        : (__uint_as_float(v0[j]) + __uint_as_float(v1[j])) + __uint_as_float(v2[j]);
             x[c + j] = vis ? fmaf(raw, sc[j], -mu[j]) : -CUDART_INF_F;
             exceed |= x[c + j] > th[j];
