@@ -60,6 +60,7 @@ FALLBACK_HBM_GBS = 6800.0
 # sources of each kernel (the hash ties a committed ncu summary to the code it measured)
 KERNEL_SOURCES = {
     "decode_kernel": ["decode_kernel.cuh", "device_utils.cuh", "frag_layout.h", "mask_span.h"],
+    "decode_persist_kernel": ["decode_kernel.cuh", "device_utils.cuh", "frag_layout.h", "mask_span.h"],
     "verify_kernel": ["verify_kernel.cuh", "device_utils.cuh", "frag_layout.h", "verify_layout.h", "mask_span.h"],
 }
 
@@ -312,11 +313,23 @@ class DeviceWorkload:
         ws = pf.pfkv_attention_workspace_bytes(B, T, Hq, s.num_kv_heads, s.head_dim, s.page_size, s.kv_dtype,
                                                self.max_seq_len, s.causal, s.window, 0)
         self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+        self.ws_bytes = ws
+        if ws:
+            self.ws[ws - 16:ws].fill_(0xFF)  # the range counter reads -1 until a persistent grid runs
         self.splits, self.split_tokens = pf.pfkv_attention_plan(B, T, Hq, s.num_kv_heads, s.head_dim, s.page_size,
                                                                 s.kv_dtype, self.max_seq_len, s.causal, s.window, 0)
         self.has_append = case.slot_new.size > 0
         merge = self.splits > 1 and ws > 0
         self.launches_per_step = (1 if self.has_append else 0) + 1 + (1 if merge else 0)
+
+    def kernel(self):
+        """The attention kernel the calls ran. The persistent decode grid (large ragged batches)
+        is the one that writes the workspace's range counter (its last 16 bytes, -1 until then)."""
+        base = kernel_of(self.case.spec)
+        if base != "decode_kernel" or not self.ws_bytes:
+            return base
+        ctr = int(self.ws[self.ws_bytes - 16:self.ws_bytes - 12].view(self.torch.int32).item())
+        return "decode_persist_kernel" if ctr >= 0 else base
 
     def append_step(self):
         s = self.case.spec
@@ -386,10 +399,9 @@ def is_prefill(spec) -> bool:
     return spec.num_q_tokens > 16
 
 
-def roofline_obj(case, wid, dec_ms, peak, peak_kind):
+def roofline_obj(case, wid, dec_ms, peak, peak_kind, kernel):
     """The decode call (decode/verify kernel + merge) against the HBM copy peak; a prefill chunk
     (dense: thousands of query rows per key) against the measured bf16 tensor peak."""
-    kernel = kernel_of(case.spec)
     dec_avg = sum(dec_ms) / len(dec_ms)
     if is_prefill(case.spec):
         tpeak, tkind = measured_tensor_peak()
@@ -431,7 +443,7 @@ def measure_workload(torch, pf, flush, case, wid, peak, peak_kind, steps, warmup
     res = {"total_ms": total_ms, "e2e_ms": e2e_ms, "nbytes": nbytes, "dec_ms": dec_ms,
            "splits": dw.splits, "split_tokens": dw.split_tokens, "launches": dw.launches_per_step,
            "io": (bi, bo), "clocks": clk,
-           "roofline": roofline_obj(case, wid, dec_ms, peak, peak_kind)}
+           "roofline": roofline_obj(case, wid, dec_ms, peak, peak_kind, dw.kernel())}
     del dw
     torch.cuda.empty_cache()
     return res

@@ -188,11 +188,18 @@ PFKV_API pfkv_status pfkv_decode_plan(int num_seqs, int num_q_tokens, int num_q_
  * num_q_heads:
  *   float o_part[rows][S][head_dim]   at offset 0
  *   float lse_part[rows][S]           right after it
+ *   int   range_counter               at the next 16-byte boundary, then
+ *                                     12 bytes of padding
  * Row index = (b * num_q_tokens + t) * num_q_heads + h. For a row whose
  * sequence was split, o_part[row][s] is the attention output of range s
  * normalised by its own weight sum and lse_part[row][s] its natural-log
  * LSE (-inf when the range holds no key visible to the row); rows of
- * sequences that were not split are not written.
+ * sequences that were not split are not written. range_counter serves the
+ * persistent grid that large ragged decode batches run on (one wave of CTAs
+ * taking the key ranges that exist, one after another, instead of one CTA
+ * per range of the longest allowed sequence): the call zeroes it on the
+ * stream before that grid starts, and afterwards it holds the number of
+ * claims made. Nothing in the workspace needs to start at zero.
  */
 PFKV_API size_t pfkv_decode_workspace_bytes(int num_seqs, int num_q_tokens, int num_q_heads,
                                    int num_kv_heads, int head_dim, int page_size,

@@ -12,4 +12,13 @@ int decode_smem_e5m2(const DecodeLaunch& cfg, int ncw) { return decode_smem_kv<k
 
 int decode_ctas_e5m2(const DecodeLaunch& cfg, int ncw) { return decode_ctas_kv<kKvE5m2>(cfg, ncw); }
 
+cudaError_t launch_decode_persist_e5m2(const DecodeLaunch& cfg, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                       const DecodeParams& p, int ctas, cudaStream_t stream) {
+  return launch_persist_kv<kKvE5m2>(cfg, tmk, tmv, p, ctas, stream);
+}
+
+int decode_persist_ctas_e5m2(const DecodeLaunch& cfg, int ncw, int num_seqs) {
+  return persist_ctas_kv<kKvE5m2>(cfg, ncw, num_seqs);
+}
+
 }  // namespace pfkv

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -323,12 +324,18 @@ pfkv_status make_plan(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_k
   return PFKV_OK;
 }
 
-size_t workspace_for(const Plan& pl, int num_seqs, int T, int Hq, int D) {
-  if (pl.splits <= 1) return 0;
+// Split partials (o_part, lse_part), then the persistent grid's range counter at the next
+// 16-byte boundary.
+size_t counter_offset(const Plan& pl, int num_seqs, int T, int Hq, int D) {
   const size_t rows = static_cast<size_t>(num_seqs) * T * Hq;
   const size_t o = rows * pl.splits * D * sizeof(float);
   const size_t l = rows * pl.splits * sizeof(float);
-  return o + l;
+  return (o + l + 15) & ~static_cast<size_t>(15);
+}
+
+size_t workspace_for(const Plan& pl, int num_seqs, int T, int Hq, int D) {
+  if (pl.splits <= 1) return 0;
+  return counter_offset(pl, num_seqs, T, Hq, D) + 16;
 }
 
 // The decode entry points keep their contract: causal, no window, 1..16 query tokens whose rows
@@ -450,10 +457,36 @@ pfkv_status attention_impl(void* out, float* lse, const void* q, const void* k_c
   p.window = pl.window;
   p.slab_tokens = pl.slab_tokens;
   p.num_slabs = pl.num_slabs;
+  p.work_ctr = nullptr;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   dim3 grid(pl.splits, num_kv_heads * pl.num_slabs, num_seqs);
-  if (pl.tc) {
+  // A grid of more than two waves, sized for the longest sequence the call allows, holds many
+  // CTAs without work when the batch is ragged (each still takes an SM slot for a few
+  // microseconds): one-slab decode then runs as one wave of CTAs that claim the ranges that exist.
+  int persist_ctas = 0;
+  if (!pl.tc && pl.num_slabs == 1 && pl.cfg.nt == 1 && pl.splits > 1 && num_seqs <= kMaxPersistSeqs) {
+    int sms;
+    e = sm_count(dev, &sms);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    const long long ctas = static_cast<long long>(num_seqs) * num_kv_heads * pl.splits;
+    const int occ = ctas_per_sm(dev, pl.cfg, pl.ncw, false, 0);
+    if (ctas > 2LL * sms * occ) {
+      const int pocc = kv == kKvFp16 ? decode_persist_ctas_fp16(pl.cfg, pl.ncw, num_seqs)
+                                     : (kv == kKvE4m3 ? decode_persist_ctas_e4m3(pl.cfg, pl.ncw, num_seqs)
+                                                      : decode_persist_ctas_e5m2(pl.cfg, pl.ncw, num_seqs));
+      persist_ctas = static_cast<int>(std::min<long long>(static_cast<long long>(sms) * pocc, ctas));
+    }
+  }
+  if (persist_ctas > 0) {
+    p.work_ctr = reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                        counter_offset(pl, num_seqs, num_q_tokens, num_q_heads, head_dim));
+    e = cudaMemsetAsync(p.work_ctr, 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(e, "range counter reset");
+    e = kv == kKvFp16 ? launch_decode_persist_fp16(pl.cfg, tmk, tmv, p, persist_ctas, s)
+                      : (kv == kKvE4m3 ? launch_decode_persist_e4m3(pl.cfg, tmk, tmv, p, persist_ctas, s)
+                                       : launch_decode_persist_e5m2(pl.cfg, tmk, tmv, p, persist_ctas, s));
+  } else if (pl.tc) {
     e = kv == kKvE4m3 ? launch_verify_e4m3(head_dim, pl.nmax, tmk, tmv, p, grid, s, nullptr)
                       : launch_verify_e5m2(head_dim, pl.nmax, tmk, tmv, p, grid, s, nullptr);
   } else {

@@ -18,6 +18,9 @@ constexpr unsigned kDevErrBlockId = 0x2u;
 constexpr unsigned kDevErrSeqLen = 0x4u;
 constexpr unsigned kDevErrTimeout = 0x8u;
 
+// sequences of one call that the persistent decode grid takes (lengths and item prefix in shared memory)
+constexpr int kMaxPersistSeqs = 1024;
+
 struct DecodeParams {
   const __half* q;
   __half* out;
@@ -50,6 +53,8 @@ struct DecodeParams {
   int window;       // > 0: query t sees no key W or more positions before its own (0: no window)
   int slab_tokens;  // query tokens per CTA
   int num_slabs;    // ceil(T / slab_tokens)
+  // persistent decode grid: the next unclaimed range (zeroed by the call before the launch)
+  int* work_ctr;
 };
 
 struct DecodeLaunch {
@@ -88,6 +93,17 @@ cudaError_t launch_decode_e5m2(const DecodeLaunch&, const CUtensorMap&, const CU
 int decode_ctas_fp16(const DecodeLaunch&, int ncw);
 int decode_ctas_e4m3(const DecodeLaunch&, int ncw);
 int decode_ctas_e5m2(const DecodeLaunch&, int ncw);
+// The persistent grid of the same kernel (one row tile per warp, one query slab, at most
+// kMaxPersistSeqs sequences): ctas CTAs take the ranges from p.work_ctr, which must read 0.
+cudaError_t launch_decode_persist_fp16(const DecodeLaunch&, const CUtensorMap&, const CUtensorMap&,
+                                       const DecodeParams&, int ctas, cudaStream_t);
+cudaError_t launch_decode_persist_e4m3(const DecodeLaunch&, const CUtensorMap&, const CUtensorMap&,
+                                       const DecodeParams&, int ctas, cudaStream_t);
+cudaError_t launch_decode_persist_e5m2(const DecodeLaunch&, const CUtensorMap&, const CUtensorMap&,
+                                       const DecodeParams&, int ctas, cudaStream_t);
+int decode_persist_ctas_fp16(const DecodeLaunch&, int ncw, int num_seqs);
+int decode_persist_ctas_e4m3(const DecodeLaunch&, int ncw, int num_seqs);
+int decode_persist_ctas_e5m2(const DecodeLaunch&, int ncw, int num_seqs);
 
 // verify_e4m3.cu / verify_e5m2.cu: tcgen05 grouped verify (FP8 caches). nmax = rows padded
 // to 32/48/64. With ctas_out non-null nothing is launched: it receives the CTAs per SM.
