@@ -199,7 +199,8 @@ PFKV_API pfkv_status pfkv_decode_plan(int num_seqs, int num_q_tokens, int num_q_
  * taking the key ranges that exist, one after another, instead of one CTA
  * per range of the longest allowed sequence): the call zeroes it on the
  * stream before that grid starts, and afterwards it holds the number of
- * claims made. Nothing in the workspace needs to start at zero.
+ * key ranges the grid processed. Nothing in the workspace needs to start
+ * at zero.
  */
 PFKV_API size_t pfkv_decode_workspace_bytes(int num_seqs, int num_q_tokens, int num_q_heads,
                                    int num_kv_heads, int head_dim, int page_size,

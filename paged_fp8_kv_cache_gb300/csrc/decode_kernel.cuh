@@ -791,9 +791,9 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
 }
 
 // One wave of CTAs over the items that have work. The items of sequence b are its (KV head,
-// range) pairs, numbered b-major from prefix[b]; the CTAs take item numbers from a counter the
-// call zeroed. The producer warp claims them and hands each to the consumer warps through a
-// two-slot mailbox; the copy ring runs on across items.
+// range) pairs, numbered b-major from prefix[b]; CTA c starts with item c and then takes item
+// numbers from a counter the call zeroed. The producer warp claims them and hands each to the
+// consumer warps through a two-slot mailbox; the copy ring runs on across items.
 // (head dim 128: registers for three CTAs per SM, as many as its shared memory allows)
 template <int D, int KV, int NT>
 __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? (D == 128 ? 3 : 2) : 1)
@@ -884,11 +884,15 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? (D == 128 ? 3 :
       prefetch_tensormap(&tmv);
     }
     for (int k = 0;; ++k) {
-      // claimed once the previous item's copies are all issued: the consumers still have a ring
-      // of stages to work through while the claim and the first page ids are fetched
-      int i = 0;
-      if (lane == 0) i = atomicAdd(p.work_ctr, 1);
-      i = __shfl_sync(0xffffffffu, i, 0);
+      // The first item is the CTA's own index; later ones are claimed once the previous item's
+      // copies are all issued (the consumers still have a ring of stages to work through while
+      // the claim and the first page ids are fetched). Each CTA that had a first item makes one
+      // claim past the end, so the counter ends at the number of items.
+      int i = static_cast<int>(blockIdx.x);
+      if (k > 0) {
+        if (lane == 0) i = static_cast<int>(gridDim.x) + atomicAdd(p.work_ctr, 1);
+        i = __shfl_sync(0xffffffffu, i, 0);
+      }
       // mailbox slot k & 1 is free once the consumers read item k - 2 (sound: this warp waited for
       // that barrier's previous phase, of item k - 4, before writing item k - 2)
       if (k >= 2) {
