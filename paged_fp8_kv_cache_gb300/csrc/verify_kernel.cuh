@@ -254,8 +254,9 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
   const int split = blockIdx.x, b = blockIdx.z;
-  const int kvh = blockIdx.y % p.num_kv_heads;
-  const int slab = p.num_slabs - 1 - static_cast<int>(blockIdx.y) / p.num_kv_heads;  // longest slabs first
+  // KV head major (CTAs running together share one head's keys in L2), longest slabs first
+  const int kvh = blockIdx.y / p.num_slabs;
+  const int slab = p.num_slabs - 1 - static_cast<int>(blockIdx.y) % p.num_slabs;
 
   // launched with programmatic stream serialisation: wait for the preceding grid first
   asm volatile("griddepcontrol.wait;" ::: "memory");
