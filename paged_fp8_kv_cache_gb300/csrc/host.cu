@@ -315,6 +315,25 @@ pfkv_status make_plan(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_k
     const int need = (long_ranges && units < sms) ? 1 : static_cast<int>((span + max_keys - 1) / max_keys);
     const int k = base > 0 ? (need + base - 1) / base : 1;
     want = base * (k > 1 ? k : 1);
+    // Tensor-core calls with units for a wave or more already (prefill chunks: a unit per query
+    // slab): the ranges only shorten the CTAs of the last wave, and each costs a partial per
+    // row and a merge term. Take the count, up to the bound, whose waves are fullest per unit of
+    // work, each range past the first counted 1.15 % dearer (2048-token chunk over 128K keys,
+    // 820 units: 9671 / 9299 / 9605 / 9464 / 9443 us at 1 / 2 / 3 / 4 / 5 ranges).
+    if (pl->tc && units >= sms * occ && want > 1) {
+      const long long slots = static_cast<long long>(sms) * occ;
+      double best = 0.0;
+      int pick = 1;
+      for (int s = 1; s <= want; ++s) {
+        const long long waves = (static_cast<long long>(units) * s + slots - 1) / slots;
+        const double cost = static_cast<double>(waves) / s * (1.0 + 0.0115 * (s - 1));
+        if (s == 1 || cost < best) {
+          best = cost;
+          pick = s;
+        }
+      }
+      want = pick;
+    }
   }
   if (want < 1) want = 1;
   if (want > tiles) want = tiles;
