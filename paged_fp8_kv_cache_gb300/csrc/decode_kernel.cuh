@@ -72,12 +72,12 @@ constexpr int decode_smem_bytes(int ncw) {
 }
 
 // The persistent kernel: ring | (m, l) | full[NS], empty[NS] | item_full[2], item_free[2], the
-// consumers' rendezvous | item slots[2] | lengths[B] | item prefix[B + 1]. (Its combine buffer is
-// the ring slot of each item's last stage.)
+// consumers' rendezvous | item slots[2] | lengths[B] | ranges[B] | item prefix[B + 1]. (Its
+// combine buffer is the ring slot of each item's last stage.)
 template <int D, int KV, int NT>
 constexpr int persist_smem_bytes(int ncw, int num_seqs) {
   using S = DecodeShape<D, KV>;
-  return S::NS * S::STAGE + ncw * 8 * NT * 8 + (2 * S::NS + 5) * 8 + 8 + (2 * num_seqs + 1) * 4;
+  return S::NS * S::STAGE + ncw * 8 * NT * 8 + (2 * S::NS + 5) * 8 + 8 + (3 * num_seqs + 1) * 4;
 }
 
 // One unit of work: a key range of one (sequence, KV head, slab).
@@ -791,9 +791,12 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? 2 : 1)
                                      warp, lane, ncw);
 }
 
-// One wave of CTAs over the items that have work. The items of sequence b are its (KV head,
-// range) pairs, numbered b-major from prefix[b]; CTA c starts with item c and then takes item
-// numbers from a counter the call zeroed. The producer warp claims them and hands each to the
+// sequences whose last ranges the persistent grid orders by length
+constexpr int kSortSeqs = 256;
+
+// One wave of CTAs over the items that have work: the (sequence, KV head, range) triples, full
+// ranges first (see decode_item below); CTA c starts with item c and then takes item numbers
+// from a counter the call zeroed. The producer warp claims them and hands each to the
 // consumer warps through a two-slot mailbox; the copy ring runs on across items.
 // (head dim 128: registers for three CTAs per SM, as many as its shared memory allows)
 template <int D, int KV, int NT>
@@ -818,7 +821,8 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? (D == 128 ? 3 :
   uint64_t* cons_bar = item_free + 2;   // the consumer warps' rendezvous
   int* item_slot = reinterpret_cast<int*>(cons_bar + 1);  // [2] mailbox
   int* lens = item_slot + 2;                              // [B] validated lengths
-  int* prefix = lens + B;                                 // [B + 1] first item of sequence b
+  int* nsp = lens + B;                                    // [B] ranges per KV head of sequence b
+  int* prefix = nsp + B;                                  // [B + 1] first leading item of sequence b
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -834,16 +838,17 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? (D == 128 ? 3 :
     mbar_init(cons_bar, ncw);
     fence_barrier_init();
   }
-  // the lengths, and the prefix of the items per sequence (warp 0, 32 sequences at a time)
+  // the lengths, the range counts, and the prefix of the leading items per sequence (warp 0, 32
+  // sequences at a time)
   if (warp == 0) {
     int run = 0;
     for (int base = 0; base < B; base += 32) {
       const int bb = base + lane;
-      int n = 0, cnt = 0;
+      int n = 0, cnt = 0, ns = 1;
       if (bb < B) {
         n = checked_len(p, p.seq_lens[bb], blockIdx.x == 0);
-        cnt = span_splits(slab_span(n, p.T, 0, p.slab_tokens, p.causal, p.window, kTileKeys), p.split_tokens) *
-              p.num_kv_heads;
+        ns = span_splits(slab_span(n, p.T, 0, p.slab_tokens, p.causal, p.window, kTileKeys), p.split_tokens);
+        cnt = (ns - 1) * p.num_kv_heads;
       }
       int incl = cnt;
 #pragma unroll
@@ -853,6 +858,7 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? (D == 128 ? 3 :
       }
       if (bb < B) {
         lens[bb] = n;
+        nsp[bb] = ns;
         prefix[bb + 1] = run + incl;
       }
       run += __shfl_sync(0xffffffffu, incl, 31);
@@ -860,9 +866,39 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? (D == 128 ? 3 :
     if (lane == 0) prefix[0] = 0;
   }
   __syncthreads();
-  const int total = prefix[B];
-  // item number -> (sequence, KV head, range): the last sequence whose first item is <= i
+  // Items: first every range but the last of each (sequence, KV head) -- full split_tokens
+  // ranges -- numbered sequence-major from prefix[b]; then the last ranges, Hkv per sequence,
+  // whose lengths vary, longest first (for up to kSortSeqs sequences; sequence order beyond),
+  // so that the CTAs finish on short items.
+  const int leading = prefix[B];
+  const int total = leading + B * p.num_kv_heads;
+  __shared__ int s_last[kSortSeqs], s_order[kSortSeqs];  // last-range keys; sequences by it
+  const bool sorted = B <= kSortSeqs;
+  if (sorted) {
+    for (int bb = threadIdx.x; bb < B; bb += blockDim.x) {
+      const SlabSpan sp = slab_span(lens[bb], p.T, 0, p.slab_tokens, p.causal, p.window, kTileKeys);
+      s_last[bb] = sp.hi >= sp.lo ? sp.hi - sp.base - (nsp[bb] - 1) * p.split_tokens + 1 : 0;
+    }
+    __syncthreads();
+    for (int bb = threadIdx.x; bb < B; bb += blockDim.x) {  // rank: longer first, ties by index
+      const int mine = s_last[bb];
+      int rank = 0;
+      for (int o = 0; o < B; ++o) {
+        const int t = s_last[o];
+        rank += (t > mine || (t == mine && o < bb)) ? 1 : 0;
+      }
+      s_order[rank] = bb;
+    }
+    __syncthreads();
+  }
   auto decode_item = [&](int i) -> DecodeItem {
+    if (i >= leading) {
+      const int j = i - leading;
+      const int jb = j / p.num_kv_heads;
+      const int bb = sorted ? s_order[jb] : jb;
+      return make_item(p, bb, j - jb * p.num_kv_heads, 0, nsp[bb] - 1, lens[bb]);
+    }
+    // the last sequence whose first leading item is <= i
     int lo = 0, hi = B - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -872,9 +908,9 @@ __global__ void __launch_bounds__(NT == 1 ? 160 : 288, NT == 1 ? (D == 128 ? 3 :
         hi = mid - 1;
       }
     }
-    const int nsplit = (prefix[lo + 1] - prefix[lo]) / p.num_kv_heads;
+    const int per = nsp[lo] - 1;  // leading ranges per KV head (at least 1 here)
     const int local = i - prefix[lo];
-    return make_item(p, lo, local / nsplit, 0, local % nsplit, lens[lo]);
+    return make_item(p, lo, local / per, 0, local % per, lens[lo]);
   };
 
   int g = 0;

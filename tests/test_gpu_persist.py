@@ -147,6 +147,18 @@ def test_multi_token_and_window(T, g, window):
     assert _counter(ws, r.case, r.splits) == r.ranges
 
 
+def test_many_sequences():
+    # more sequences than the grid orders by their last range's length (256): the last ranges
+    # then follow in sequence order
+    r = Ragged(_spec(_ragged(300, 1, 2000, seed=14), Hkv=2, seed=47), num_splits=4)
+    ws = _garbage(r.ws_bytes)
+    r.clear()
+    r.call(ws)
+    torch.cuda.synchronize()
+    r.check()
+    assert _counter(ws, r.case, r.splits) == r.ranges
+
+
 def test_one_workspace_across_batches():
     # two batches of different shapes take turns on one workspace, with no synchronisation
     a = Ragged(_spec(_ragged(48, 16, 5000, seed=11), seed=44))
