@@ -224,9 +224,9 @@ PFKV_API size_t pfkv_decode_workspace_bytes(int num_seqs, int num_q_tokens, int 
  * where dec() is the exact FP8 (or fp16) value of a cache element. A row
  * that sees no key gets out = 0 and lse = -inf.
  *
- *   out            device, fp16 [num_seqs * T][num_q_heads][head_dim]
- *   lse            device, float [num_seqs * T][num_q_heads]
- *   q              device, fp16 [num_seqs * T][num_q_heads][head_dim], 8-byte aligned
+ *   out            device, fp16 [num_seqs * T][num_q_heads][head_dim], 8-byte aligned
+ *   lse            device, float [num_seqs * T][num_q_heads], 4-byte aligned
+ *   q              device, fp16 [num_seqs * T][num_q_heads][head_dim], 16-byte aligned
  *   k_cache, v_cache device pools (see top of file); 16-byte aligned
  *   block_table    device, int32 [num_seqs][max_blocks_per_seq]; entries past
  *                  a sequence's last page are never read

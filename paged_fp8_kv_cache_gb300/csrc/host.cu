@@ -421,8 +421,9 @@ pfkv_status attention_impl(void* out, float* lse, const void* q, const void* k_c
     return fail(PFKV_ERR_UNSUPPORTED, "max_blocks_per_seq * page_size exceeds 2^31");
   if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15)
     return fail(PFKV_ERR_INVALID_ARG, "cache pools must be 16-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 7)
-    return fail(PFKV_ERR_INVALID_ARG, "q and out must be 8-byte aligned");
+  if (reinterpret_cast<uintptr_t>(q) & 15)
+    return fail(PFKV_ERR_INVALID_ARG, "q must be 16-byte aligned");  // the verify kernel reads 16-byte pieces
+  if (reinterpret_cast<uintptr_t>(out) & 7) return fail(PFKV_ERR_INVALID_ARG, "out must be 8-byte aligned");
   if (reinterpret_cast<uintptr_t>(lse) & 3) return fail(PFKV_ERR_INVALID_ARG, "lse must be 4-byte aligned");
   const size_t need = workspace_for(pl, num_seqs, num_q_tokens, num_q_heads, head_dim);
   if (need > 0) {

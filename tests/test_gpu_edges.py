@@ -124,3 +124,36 @@ def test_host_rejections_with_real_buffers():
         pf.pfkv_paged_attention_decode(out, lse, g.q, g.k_cache, g.v_cache, g.block_table, g.seq_lens, 1, 2, 16,
                                        "e4m3", None, None, 0.1, 3000, 1, None)
     assert ei.value.status == pf.PFKV_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kv,T,g,D", [("e5m2", 8, 6, 256), ("e4m3", 8, 6, 128), ("e4m3", 1, 4, 256), ("fp16", 2, 4, 256)])
+def test_out_8_byte_aligned_and_q_alignment_checked(kv, T, g, D):
+    # the ABI asks 8-byte alignment of out and 16-byte alignment of q: out at 8 bytes past a
+    # 16-byte boundary is served; such a q is refused on the host, before anything is enqueued
+    case = workloads.make_case(spec(kv, T, g, 2, D, 64, (700, 129, 5)))
+    kc, vc = oracle_caches(case)
+    o_ref, l_ref = oracle_attention(case, kc, vc)
+    gc = GpuCase(case)
+    n = gc.q.numel()
+    out_buf = torch.full((n + 4,), float("nan"), dtype=torch.float16, device="cuda")
+    out8 = out_buf[4:].view(gc.q.shape)
+    assert out8.data_ptr() % 16 == 8
+    lse = torch.full(gc.q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+    s = case.spec
+    msl = int(case.seq_lens.max())
+    ws = torch.empty(max(pf.pfkv_decode_workspace_bytes(case.B, T, s.num_q_heads, 2, D, 64, kv, msl, 0), 16),
+                     dtype=torch.uint8, device="cuda")
+
+    def call(q, out):
+        pf.pfkv_paged_attention_decode(out, lse, q, gc.k_cache, gc.v_cache, gc.block_table, gc.seq_lens, T, 2, 64,
+                                       kv, gc.k_scale, gc.v_scale, float(case.softmax_scale), msl, 0, ws)
+
+    call(gc.q, out8)
+    torch.cuda.synchronize()
+    assert_close(out8, lse, o_ref, l_ref)
+    q_buf = torch.empty(n + 4, dtype=torch.float16, device="cuda")
+    q8 = q_buf[4:].view(gc.q.shape)
+    assert q8.data_ptr() % 16 == 8
+    with pytest.raises(pf.PfkvError):
+        call(q8, out8)
+    assert pf.pfkv_device_errors(clear=True) == 0
