@@ -9,8 +9,8 @@ through the C ABI (paged_fp8_kv_cache_gb300.binding -> libpfkv.so).
 
 Prints ONE JSON line (rank 0). The headline workload is the q8 speculative
 verify over 2 x 256K keys (1.07 GB of FP8 KV per step: the largest workload
-of fixed size, and one of the two long-context workloads the 75 % target is
-judged on). ``value`` = algorithmic bytes of all ranks / max-over-ranks device
+of fixed size, and one of the two long-context workloads that carry the
+75 %-of-peak target). ``value`` = algorithmic bytes of all ranks / max-over-ranks device
 time of the K timed steps (inputs resident in HBM, L2 flushed between steps:
 a 256 MiB write, then a 256 MiB read, so that the step starts on a cold L2
 holding no dirty lines, whose write-back would otherwise compete with the
