@@ -159,6 +159,19 @@ def test_many_sequences():
     assert _counter(ws, r.case, r.splits) == r.ranges
 
 
+@pytest.mark.parametrize("B", [1024, 1025])
+def test_largest_batches(B):
+    # 1024 sequences is the most the persistent grid takes (lengths and item prefix in shared
+    # memory); one more runs the one-CTA-per-range grid
+    r = Ragged(_spec(_ragged(B, 1, 300, seed=15), Hkv=2, seed=48), num_splits=2, max_seq_len=512)
+    ws = _garbage(r.ws_bytes)
+    r.clear()
+    r.call(ws)
+    torch.cuda.synchronize()
+    r.check()
+    assert _counter(ws, r.case, r.splits) == (r.ranges if B <= 1024 else GARBAGE)
+
+
 def test_one_workspace_across_batches():
     # two batches of different shapes take turns on one workspace, with no synchronisation
     a = Ragged(_spec(_ragged(48, 16, 5000, seed=11), seed=44))
