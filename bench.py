@@ -441,7 +441,9 @@ def measure_workload(torch, pf, flush, case, wid, peak, peak_kind, steps, warmup
         raise RuntimeError(f"device error word set while timing workload {wid}")
     bi, bo = dw.io_bytes()
     res = {"total_ms": total_ms, "e2e_ms": e2e_ms, "nbytes": nbytes, "dec_ms": dec_ms,
-           "splits": dw.splits, "split_tokens": dw.split_tokens, "launches": dw.launches_per_step,
+           "splits": dw.splits, "split_tokens": dw.split_tokens,
+           # the persistent decode grid adds the kernel that zeroes its range counter
+           "launches": dw.launches_per_step + (1 if dw.kernel() == "decode_persist_kernel" else 0),
            "io": (bi, bo), "clocks": clk,
            "roofline": roofline_obj(case, wid, dec_ms, peak, peak_kind, dw.kernel())}
     del dw

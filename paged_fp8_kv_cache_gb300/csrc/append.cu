@@ -45,6 +45,10 @@ __global__ void __launch_bounds__(256) append_kernel(const __half* __restrict__ 
                                                      const float* __restrict__ k_scale,
                                                      const float* __restrict__ v_scale, int scale_stride,
                                                      unsigned* err) {
+  // An attention kernel launched next with programmatic stream serialisation may start its
+  // launch now: it waits (griddepcontrol.wait) for this grid to complete, and its writes to be
+  // visible, before it reads the cache.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int chunks = head_dim / 8;
   const int64_t per_tok = static_cast<int64_t>(num_kv_heads) * chunks;
   const int64_t total = per_tok * n_tok;

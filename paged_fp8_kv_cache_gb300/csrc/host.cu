@@ -258,6 +258,16 @@ pfkv_status check_shape(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv
   return PFKV_OK;
 }
 
+// Zeroes the persistent decode grid's range counter. Launched with programmatic serialisation
+// between the previous kernel on the stream (e.g. the step's append, which releases its
+// dependents at once) and the persistent grid (which waits for this one): unlike a memset node it
+// lets both launches overlap the kernel before.
+__global__ void zero_counter_kernel(int* ctr) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) *ctr = 0;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 pfkv_status make_plan(int num_seqs, int T, int Hq, int Hkv, int D, int P, pfkv_kv_dtype dtype, int mask, int window,
                       int max_seq_len, int num_splits_request, Plan* pl) {
   pfkv_status st = check_shape(num_seqs, T, Hq, Hkv, D, P, dtype, mask, window, max_seq_len, num_splits_request);
@@ -501,7 +511,7 @@ pfkv_status attention_impl(void* out, float* lse, const void* q, const void* k_c
   if (persist_ctas > 0) {
     p.work_ctr = reinterpret_cast<int*>(static_cast<char*>(workspace) +
                                         counter_offset(pl, num_seqs, num_q_tokens, num_q_heads, head_dim));
-    e = cudaMemsetAsync(p.work_ctr, 0, sizeof(int), s);
+    e = launch_pdl(zero_counter_kernel, dim3(1), dim3(32), 0, s, p.work_ctr);
     if (e != cudaSuccess) return cuda_fail(e, "range counter reset");
     e = kv == kKvFp16 ? launch_decode_persist_fp16(pl.cfg, tmk, tmv, p, persist_ctas, s)
                       : (kv == kKvE4m3 ? launch_decode_persist_e4m3(pl.cfg, tmk, tmv, p, persist_ctas, s)
