@@ -4,9 +4,10 @@
 //   M = max_s lse_s, w_s = exp(lse_s - M),
 //   out = sum_s w_s o_s / sum_s w_s, lse = M + ln(sum_s w_s).
 //
-// One CTA of 8 warps per output row; the row's parts are spread over the
-// warps, each warp keeping a running maximum, so that a row with up to 64
-// split ranges costs one memory round trip. When launched after the decode
+// One CTA per output row, of 1, 2, 4 or 8 warps (at least one per 8 parts of
+// the call, so that a row costs one memory round trip up to 64 parts, and
+// calls with many rows of few parts fit on the GPU in one wave); the row's
+// parts are spread over the warps, each warp keeping a running maximum. When launched after the decode
 // kernel with programmatic stream serialisation, the grid starts while the
 // decode kernel drains and waits (griddepcontrol.wait) before touching the
 // partials.
@@ -18,21 +19,21 @@
 
 namespace pfkv {
 
-template <int D>
-__global__ void __launch_bounds__(256) lse_merge_kernel(__half* __restrict__ out, float* __restrict__ lse,
-                                                        const float* __restrict__ o_parts,
-                                                        const float* __restrict__ lse_parts, int rows, int num_parts,
-                                                        const MergeRows mr) {
-  // One CTA (8 warps) per row. Warp w takes parts w, w+8, ...; each lane owns D/32
+template <int D, int NW>
+__global__ void __launch_bounds__(NW * 32) lse_merge_kernel(__half* __restrict__ out, float* __restrict__ lse,
+                                                            const float* __restrict__ o_parts,
+                                                            const float* __restrict__ lse_parts, int rows,
+                                                            int num_parts, const MergeRows mr) {
+  // One CTA (NW warps) per row. Warp w takes parts w, w+NW, ...; each lane owns D/32
   // consecutive output elements. A warp issues the loads (LSE and output) of up to kBatch of
   // its parts at once and keeps a running maximum with sums rescaled to it, so a row costs
-  // one memory round trip; the 8 warps' results are then rescaled to the row maximum and
+  // one memory round trip; the NW warps' results are then rescaled to the row maximum and
   // added through shared memory.
   constexpr int PER = D / 32;  // 4 or 8 floats per lane
   constexpr int kBatch = 8;
-  __shared__ float s_m[8];
-  __shared__ float s_w[8];
-  __shared__ float4 s_acc[8][D / 4];
+  __shared__ float s_m[NW];
+  __shared__ float s_w[NW];
+  __shared__ float4 s_acc[NW][D / 4];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = blockIdx.x;
   int n = num_parts;
@@ -55,12 +56,12 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(__half* __restrict__ out
   float acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-  for (int s0 = warp; s0 < n; s0 += 8 * kBatch) {
+  for (int s0 = warp; s0 < n; s0 += NW * kBatch) {
     float4 v[kBatch][PER / 4];
     float l[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
-      const int s = s0 + 8 * u;
+      const int s = s0 + NW * u;
       l[u] = -CUDART_INF_F;
       if (s < n) {
         l[u] = lp[s];
@@ -80,7 +81,7 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(__half* __restrict__ out
     for (int i = 0; i < PER; ++i) acc[i] *= sc;
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
-      if (s0 + 8 * u < n && l[u] != -CUDART_INF_F) {
+      if (s0 + NW * u < n && l[u] != -CUDART_INF_F) {
         const float w = expf(l[u] - nm);
         Ww += w;
 #pragma unroll
@@ -102,19 +103,19 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(__half* __restrict__ out
     s_w[warp] = Ww;
   }
   __syncthreads();
-  // D / 4 threads finish the float4 outputs (D = 128: 32 threads, D = 256: 64 threads)
-  if (threadIdx.x < D / 4) {
+  // the D / 4 float4 outputs (D = 128: 32, D = 256: 64), one per thread while the CTA has them
+  for (int t = threadIdx.x; t < D / 4; t += NW * 32) {
     float M = s_m[0];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) M = fmaxf(M, s_m[w]);
+    for (int w = 1; w < NW; ++w) M = fmaxf(M, s_m[w]);
     float Wt = 0.f;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -CUDART_INF_F) {
 #pragma unroll
-      for (int w = 0; w < 8; ++w) {
+      for (int w = 0; w < NW; ++w) {
         const float f = (s_m[w] == -CUDART_INF_F) ? 0.f : expf(s_m[w] - M);
         Wt += f * s_w[w];
-        const float4 x = s_acc[w][threadIdx.x];
+        const float4 x = s_acc[w][t];
         a.x += f * x.x;
         a.y += f * x.y;
         a.z += f * x.z;
@@ -128,9 +129,30 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(__half* __restrict__ out
     uint2 packed;
     packed.x = *reinterpret_cast<const uint32_t*>(&h01);
     packed.y = *reinterpret_cast<const uint32_t*>(&h23);
-    *reinterpret_cast<uint2*>(out + static_cast<int64_t>(r) * D + 4 * threadIdx.x) = packed;
-    if (threadIdx.x == 0 && lse != nullptr) lse[r] = has ? M + logf(Wt) : -CUDART_INF_F;
+    *reinterpret_cast<uint2*>(out + static_cast<int64_t>(r) * D + 4 * t) = packed;
+    if (t == 0 && lse != nullptr) lse[r] = has ? M + logf(Wt) : -CUDART_INF_F;
   }
+}
+
+// Warps per row: one per 8 parts (kBatch), at most 8.
+template <int D>
+cudaError_t launch_merge_d(const cudaLaunchConfig_t& base, __half* out, float* lse, const float* o_parts,
+                           const float* lse_parts, int rows, int num_parts, const MergeRows& mr) {
+  cudaLaunchConfig_t cfg = base;
+  if (num_parts <= 8) {
+    cfg.blockDim = dim3(32);
+    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<D, 1>, out, lse, o_parts, lse_parts, rows, num_parts, mr);
+  }
+  if (num_parts <= 16) {
+    cfg.blockDim = dim3(64);
+    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<D, 2>, out, lse, o_parts, lse_parts, rows, num_parts, mr);
+  }
+  if (num_parts <= 32) {
+    cfg.blockDim = dim3(128);
+    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<D, 4>, out, lse, o_parts, lse_parts, rows, num_parts, mr);
+  }
+  cfg.blockDim = dim3(256);
+  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<D, 8>, out, lse, o_parts, lse_parts, rows, num_parts, mr);
 }
 
 // Generic head dims (multiples of 4 up to 1024, standalone entry point only):
@@ -186,7 +208,6 @@ cudaError_t launch_lse_merge(__half* out, float* lse, const float* o_parts, cons
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(rows));
-  cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -194,9 +215,8 @@ cudaError_t launch_lse_merge(__half* out, float* lse, const float* o_parts, cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (head_dim == 128)
-    return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128>, out, lse, o_parts, lse_parts, rows, num_parts, mr);
-  return cudaLaunchKernelEx(&cfg, lse_merge_kernel<256>, out, lse, o_parts, lse_parts, rows, num_parts, mr);
+  if (head_dim == 128) return launch_merge_d<128>(cfg, out, lse, o_parts, lse_parts, rows, num_parts, mr);
+  return launch_merge_d<256>(cfg, out, lse, o_parts, lse_parts, rows, num_parts, mr);
 }
 
 }  // namespace pfkv
