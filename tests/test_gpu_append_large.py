@@ -16,6 +16,7 @@ pytestmark = pytest.mark.gpu
     ("e4m3", 32768, 4, 256, 2048, False),   # 33.5M elements per pool in one call
     ("e5m2", 40000, 8, 128, 16, True),      # 41M elements, one scale per KV head
     ("fp16", 65536, 4, 128, 64, False),    # 33.5M elements
+    ("e4m3", 80000, 3, 96, 48, False),     # 23M elements: page size and head dim not powers of two
 ])
 def test_single_large_append_is_bit_exact(pflib, kv, n_tok, hkv, d, page, per_head):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
