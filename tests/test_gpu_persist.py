@@ -135,6 +135,19 @@ def test_empty_and_tiny_sequences_more_ctas_than_ranges():
     assert _counter(ws, r.case, r.splits) == r.ranges
 
 
+def test_sequences_shorter_than_the_query_block():
+    # q4 rows of sequences with 0..3 keys (no key or only some of the block's own) among longer
+    # ones, on the persistent grid
+    ctx = [0, 0, 1, 2, 3, 1, 0, 2] * 6 + [3000, 1500]
+    r = Ragged(_spec(ctx, T=4, g=2, seed=49), num_splits=8)
+    ws = _garbage(r.ws_bytes)
+    r.clear()
+    r.call(ws)
+    torch.cuda.synchronize()
+    r.check()
+    assert _counter(ws, r.case, r.splits) == r.ranges
+
+
 @pytest.mark.parametrize("T,g,window", [(2, 4, 0), (1, 8, 1000), (4, 2, 300)])
 def test_multi_token_and_window(T, g, window):
     r = Ragged(_spec(_ragged(40, 4, 6000, seed=7 + T), T=T, g=g, seed=43), causal=True, window=window,
