@@ -260,6 +260,28 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
 
   // launched with programmatic stream serialisation: wait for the preceding grid first
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Up to 48 rows the slab's Q rows (fp16) are copied into the P^T buffers, not yet in use, with
+  // asynchronous 16-byte copies issued by every thread at once, so that the prologue waits for one
+  // memory round trip instead of one per row of each warp (a slab's query tokens do not depend
+  // on the sequence length). (The 64-row kernels keep per-warp loads: their register-bound code
+  // measured slower with any change to the prologue.)
+  constexpr bool QSTAGE = NMAX <= 48;
+  if constexpr (QSTAGE) {
+    static_assert(NMAX * D * 2 <= 2 * S::PT_BYTES, "Q staging fits the P^T buffers");
+    const int ts0q = slab * p.slab_tokens;
+    const int rows = (min(ts0q + p.slab_tokens, p.T) - ts0q) * p.G;
+    constexpr int CH = D / 8;  // 16-byte chunks per row
+    for (int idx = threadIdx.x; idx < rows * CH; idx += blockDim.x) {
+      const int r = idx / CH, c = idx - r * CH;
+      const int tl = r / p.G, j = r - tl * p.G;
+      const __half* src =
+          p.q + ((static_cast<size_t>(b) * p.T + ts0q + tl) * p.num_q_heads + kvh * p.G + j) * D + c * 8;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem + S::OFF_PT + r * (D * 2) + c * 16)),
+                   "l"(src)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
   int N = p.seq_lens[b];
   {
     const int cap = min(p.max_seq_len, p.max_blocks * p.page_size);
@@ -270,7 +292,10 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
   }
   const SlabSpan sp = slab_span(N, p.T, slab, p.slab_tokens, p.causal, p.window, KT);
   const int nsplit_b = span_splits(sp, p.split_tokens);
-  if (split >= nsplit_b) return;
+  if (split >= nsplit_b) {
+    if constexpr (QSTAGE) asm volatile("cp.async.wait_all;" ::: "memory");  // no copy lands after the CTA left
+    return;
+  }
   const int R = (sp.ts1 - sp.ts0) * p.G;  // query rows of this slab
   const int t0 = sp.base + split * p.split_tokens;
   const int t1 = sp.hi >= sp.lo ? min(sp.hi + 1, t0 + p.split_tokens) : t0;
@@ -339,6 +364,10 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
   const float kscale = p.k_scale[kvh * p.scale_stride], vscale = p.v_scale[kvh * p.scale_stride];
   const float sc2 = p.softmax_scale * kscale * 1.4426950408889634f;
   // Q -> three E4M3 terms in shared memory (K-major, 128B swizzle), one warp per row; padded rows zero
+  if constexpr (QSTAGE) {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();  // every thread's Q copies have landed
+  }
   {
     constexpr int PER_LANE = D / 32;  // 8 (D = 256) or 4 (D = 128) consecutive dims per lane
     for (int r = warp; r < NMAX; r += kVerifyWarps) {
@@ -346,8 +375,9 @@ __global__ void __launch_bounds__(kVerifyWarps * 32, 1)
       float mx = 0.f;
       if (r < R) {
         const int tl = r / p.G, j = r - tl * p.G;
-        const __half* src =
-            p.q + ((static_cast<size_t>(b) * p.T + sp.ts0 + tl) * p.num_q_heads + kvh * p.G + j) * D + lane * PER_LANE;
+        const __half* src = QSTAGE ? reinterpret_cast<const __half*>(smem + S::OFF_PT + r * (D * 2)) + lane * PER_LANE
+                                   : p.q + ((static_cast<size_t>(b) * p.T + sp.ts0 + tl) * p.num_q_heads + kvh * p.G + j) * D +
+                                         lane * PER_LANE;
         if constexpr (PER_LANE == 8) {
           const uint4 v = *reinterpret_cast<const uint4*>(src);
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
