@@ -8,8 +8,6 @@ cudaError_t launch_decode_e4m3(const DecodeLaunch& cfg, const CUtensorMap& tmk, 
   return launch_decode_kv<kKvE4m3>(cfg, tmk, tmv, p, grid, stream);
 }
 
-int decode_smem_e4m3(const DecodeLaunch& cfg, int ncw) { return decode_smem_kv<kKvE4m3>(cfg, ncw); }
-
 int decode_ctas_e4m3(const DecodeLaunch& cfg, int ncw) { return decode_ctas_kv<kKvE4m3>(cfg, ncw); }
 
 cudaError_t launch_decode_persist_e4m3(const DecodeLaunch& cfg, const CUtensorMap& tmk, const CUtensorMap& tmv,

@@ -8,8 +8,6 @@ cudaError_t launch_decode_e5m2(const DecodeLaunch& cfg, const CUtensorMap& tmk, 
   return launch_decode_kv<kKvE5m2>(cfg, tmk, tmv, p, grid, stream);
 }
 
-int decode_smem_e5m2(const DecodeLaunch& cfg, int ncw) { return decode_smem_kv<kKvE5m2>(cfg, ncw); }
-
 int decode_ctas_e5m2(const DecodeLaunch& cfg, int ncw) { return decode_ctas_kv<kKvE5m2>(cfg, ncw); }
 
 cudaError_t launch_decode_persist_e5m2(const DecodeLaunch& cfg, const CUtensorMap& tmk, const CUtensorMap& tmv,

@@ -8,8 +8,6 @@ cudaError_t launch_decode_fp16(const DecodeLaunch& cfg, const CUtensorMap& tmk, 
   return launch_decode_kv<kKvFp16>(cfg, tmk, tmv, p, grid, stream);
 }
 
-int decode_smem_fp16(const DecodeLaunch& cfg, int ncw) { return decode_smem_kv<kKvFp16>(cfg, ncw); }
-
 int decode_ctas_fp16(const DecodeLaunch& cfg, int ncw) { return decode_ctas_kv<kKvFp16>(cfg, ncw); }
 
 cudaError_t launch_decode_persist_fp16(const DecodeLaunch& cfg, const CUtensorMap& tmk, const CUtensorMap& tmv,

@@ -106,13 +106,6 @@ cudaError_t launch_decode_kv(const DecodeLaunch& cfg, const CUtensorMap& tmk, co
 }
 
 template <int KV>
-int decode_smem_kv(const DecodeLaunch& cfg, int ncw) {
-  if (cfg.head_dim == 128)
-    return (cfg.nt == 1 ? decode_smem_bytes<128, KV, 1>(ncw) : decode_smem_bytes<128, KV, 2>(ncw)) + 1024;
-  return (cfg.nt == 1 ? decode_smem_bytes<256, KV, 1>(ncw) : decode_smem_bytes<256, KV, 2>(ncw)) + 1024;
-}
-
-template <int KV>
 int decode_ctas_kv(const DecodeLaunch& cfg, int ncw) {
   if (cfg.head_dim == 128) return cfg.nt == 1 ? ctas_one<128, KV, 1>(ncw) : ctas_one<128, KV, 2>(ncw);
   return cfg.nt == 1 ? ctas_one<256, KV, 1>(ncw) : ctas_one<256, KV, 2>(ncw);
