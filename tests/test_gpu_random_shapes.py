@@ -2,7 +2,9 @@
 dim, page size, GQA group, query tokens (decode, verify and prefill slabs), ragged and empty
 sequences, causal or not, sliding windows and forced split counts drawn together, so that
 combinations no hand-written case names (a windowed prefill on the fp16 cache, a 3-head group at
-13 tokens on 32-token pages, ...) meet the same 2e-3 / 1e-4 bar as the rest."""
+13 tokens on 32-token pages, ...) meet the same 2e-3 / 1e-4 bar as the rest. A second set draws
+large ragged decode batches with random masks and split counts, which run on the persistent grid
+when their one-CTA-per-range grid would exceed two waves."""
 
 import numpy as np
 import pytest
@@ -78,3 +80,30 @@ def test_random_shape_matches_oracle(c):
     torch.cuda.synchronize()
     assert np.array_equal(g.k_cache.cpu().numpy().view(np.uint8), kc.view(np.uint8))
     assert_close(out, lse, o_ref, l_ref)
+
+
+def _draw_batch(i):
+    # large ragged decode batches (one row tile per KV head, so that the call may run the
+    # persistent grid) with random masks and split counts
+    rng = np.random.Generator(np.random.PCG64(9500 + i))
+    kv = ["e4m3", "e5m2", "fp16"][rng.integers(3)]
+    D = [128, 256][rng.integers(2)]
+    P = [16, 64, 2048][rng.integers(3)]
+    Hkv = [2, 4, 8][rng.integers(3)]
+    g = [1, 2, 4, 8][rng.integers(4)]
+    T = int(rng.integers(1, 8 // g + 1))
+    B = int(rng.integers(40, 97))
+    contexts = tuple(int(c) for c in np.exp(rng.uniform(0, np.log(3000), size=B)).astype(np.int64) - 1)
+    causal = bool(rng.random() < 0.7)
+    window = 0 if rng.random() < 0.6 else int(rng.integers(1, 1500))
+    splits = int(rng.integers(2, 9))
+    return dict(kv=kv, D=D, P=P, Hkv=Hkv, g=g, T=T, contexts=contexts, causal=causal, window=window,
+                splits=splits, seed=9500 + i)
+
+
+BATCHES = [_draw_batch(i) for i in range(16)]
+
+
+@pytest.mark.parametrize("c", BATCHES, ids=[_id(c) for c in BATCHES])
+def test_random_ragged_batch_matches_oracle(c):
+    test_random_shape_matches_oracle(c)
