@@ -25,8 +25,11 @@ def _lib(pflib):
     assert pf.pfkv_device_errors(clear=True) == 0
 
 
-# the mixed batch (one new token per sequence) and the q8 verifier (the 8 drafts' K/V appended)
-@pytest.mark.parametrize("cfg,contexts,new", [(5, ("loguniform", 30, 900, 12), 1), (4, (700, 300), 8)])
+# the mixed batch (one new token per sequence; 12 sequences on the one-CTA-per-range grid, 64 on
+# the persistent grid, whose step chains append, counter reset and attention by programmatic
+# launch) and the q8 verifier (the 8 drafts' K/V appended)
+@pytest.mark.parametrize("cfg,contexts,new", [(5, ("loguniform", 30, 900, 12), 1), (5, ("loguniform", 30, 3000, 64), 1),
+                                              (4, (700, 300), 8)])
 def test_append_and_decode_replayed_from_a_graph(cfg, contexts, new):
     case = workloads.make_case(workloads.small_spec(cfg, contexts=contexts, append_new=new))
     s = case.spec
